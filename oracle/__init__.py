@@ -1,0 +1,172 @@
+"""fp64 CPU oracle for frame-aligned block-sparse attention -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+arm of ``bench.py`` may import this package.  The CUDA library never calls it,
+and it shares no code with the CUDA path (the one shared module is the seeded
+input generator, which holds none of the method's arithmetic).
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, compiled with gcc and
+``-ffp-contract=off``); this file only compiles it and marshals numpy arrays.
+Every function states the passage it follows; see the header of ``oracle.c``.
+
+Pins (tests/test_oracle.py, CPU only): brute-force dense attention with an
+explicit -inf mask, torch's fp64 scaled_dot_product_attention on an all-ones
+mask, closed forms (q = 0, equal keys, constant values, one dominant key,
+permutation inside a block, two-key softmax), the Cauchy-Schwarz invariant,
+shift invariance of the softmax (bound shift vs max shift), and the fp32 norm
+recipe against fp64 norms and exact special cases.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+
+def build(force: bool = False) -> str:
+    src = os.path.join(_HERE, "oracle.c")
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-fno-fast-math", "-o", _LIB_PATH, src, "-lm", "-lpthread"])
+    return _LIB_PATH
+
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+        lib.orc_allowed_csr.restype = i32
+        lib.orc_allowed_csr.argtypes = [i32, _P, _P, _P]
+        lib.orc_attention.restype = None
+        lib.orc_attention.argtypes = [i32, i32, i64, i32, i32, _P, _P, _P, _P, f64, i64, _P, _P, _P, _P, _P, i32]
+        lib.orc_row_norms_f64.restype = None
+        lib.orc_row_norms_f64.argtypes = [i64, i32, _P, _P]
+        lib.orc_row_bounds_f64.restype = None
+        lib.orc_row_bounds_f64.argtypes = [i32, i64, i32, _P, f64, _P, _P, _P]
+        lib.orc_row_norms_f32.restype = None
+        lib.orc_row_norms_f32.argtypes = [i64, i32, _P, _P]
+        lib.orc_block_max_f32.restype = None
+        lib.orc_block_max_f32.argtypes = [i32, i32, i32, _P, _P]
+        lib.orc_row_bounds_f32.restype = None
+        lib.orc_row_bounds_f32.argtypes = [i32, i64, i32, _P, f32, _P, _P, _P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _u16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, "bf16 tensors are passed as uint16 bit patterns"
+    return a
+
+
+def n_threads() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def allowed_csr(mask: np.ndarray):
+    """(row_ptr[nb+1], col_idx[nnz]) of the allowed key blocks, ascending."""
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    nb = m.shape[0]
+    assert m.shape == (nb, nb)
+    row_ptr = np.zeros(nb + 1, dtype=np.int32)
+    col_idx = np.zeros(max(nb * nb, 1), dtype=np.int32)
+    nnz = _load().orc_allowed_csr(nb, _ptr(m), _ptr(row_ptr), _ptr(col_idx))
+    return row_ptr, col_idx[:nnz].copy()
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, block: int, scale: float,
+              rows: Optional[np.ndarray] = None, shift: Optional[np.ndarray] = None,
+              nthreads: Optional[int] = None):
+    """fp64 masked softmax attention.
+
+    q, k, v: uint16 bf16 bits [B,H,L,D].  rows: global row ids into B*H*L (None = all).
+    Returns (O [nrows, D] fp64, LSE [nrows], l [nrows]) where l = sum_j exp(S_ij - shift_i)
+    (shift = row max when ``shift`` is None)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, H, L, D = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and L % block == 0
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    nrows = B * H * L if rows is None else len(rows)
+    rws = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    sh = None if shift is None else np.ascontiguousarray(shift, dtype=np.float64)
+    if sh is not None:
+        assert sh.shape == (nrows,)
+    out = np.empty((nrows, D), dtype=np.float64)
+    lse = np.empty(nrows, dtype=np.float64)
+    lsum = np.empty(nrows, dtype=np.float64)
+    _load().orc_attention(B, H, L, D, block, _ptr(m), _ptr(q), _ptr(k), _ptr(v), float(scale), nrows,
+                          _ptr(rws), _ptr(sh), _ptr(out), _ptr(lse), _ptr(lsum),
+                          nthreads or n_threads())
+    return out, lse, lsum
+
+
+def row_norms_f64(x: np.ndarray) -> np.ndarray:
+    x = _u16(x)
+    D = x.shape[-1]
+    out = np.empty(x.shape[:-1], dtype=np.float64)
+    _load().orc_row_norms_f64(x.size // D, D, _ptr(x), _ptr(out))
+    return out
+
+
+def row_bounds_f64(qnorm: np.ndarray, knorm: np.ndarray, mask: np.ndarray, block: int, scale: float):
+    """M_i = scale * |q_i| * max_{j allowed} |k_j| in fp64; qnorm, knorm are [B,H,L]."""
+    qn = np.ascontiguousarray(qnorm, dtype=np.float64)
+    kn = np.ascontiguousarray(knorm, dtype=np.float64)
+    B, H, L = qn.shape
+    out = np.empty_like(qn)
+    _load().orc_row_bounds_f64(B * H, L, block, _ptr(np.ascontiguousarray(mask, dtype=np.uint8)),
+                               float(scale), _ptr(qn), _ptr(kn), _ptr(out))
+    return out
+
+
+def row_norms_f32(x: np.ndarray) -> np.ndarray:
+    """Canonical fp32 row norms (16 chunks, fmaf in order, xor-tree, sqrtf)."""
+    x = _u16(x)
+    D = x.shape[-1]
+    assert D % 16 == 0
+    out = np.empty(x.shape[:-1], dtype=np.float32)
+    _load().orc_row_norms_f32(x.size // D, D, _ptr(x), _ptr(out))
+    return out
+
+
+def block_max_f32(knorm: np.ndarray, block: int) -> np.ndarray:
+    kn = np.ascontiguousarray(knorm, dtype=np.float32)
+    B, H, L = kn.shape
+    nb = L // block
+    out = np.empty((B, H, nb), dtype=np.float32)
+    _load().orc_block_max_f32(B * H, nb, block, _ptr(kn), _ptr(out))
+    return out
+
+
+def row_bounds_f32(qnorm: np.ndarray, kmax: np.ndarray, mask: np.ndarray, block: int, scale: float):
+    qn = np.ascontiguousarray(qnorm, dtype=np.float32)
+    km = np.ascontiguousarray(kmax, dtype=np.float32)
+    B, H, L = qn.shape
+    out = np.empty_like(qn)
+    _load().orc_row_bounds_f32(B * H, L, block, _ptr(np.ascontiguousarray(mask, dtype=np.uint8)),
+                               np.float32(scale), _ptr(qn), _ptr(km), _ptr(out))
+    return out
+
+
+def metadata_f32(q: np.ndarray, k: np.ndarray, mask: np.ndarray, block: int, scale: float):
+    """(qnorm [B,H,L], kmax [B,H,nb], rowbound [B,H,L]) with the canonical fp32 recipe."""
+    qn = row_norms_f32(q)
+    kn = row_norms_f32(k)
+    km = block_max_f32(kn, block)
+    return qn, km, row_bounds_f32(qn, km, mask, block, scale)

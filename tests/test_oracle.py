@@ -1,0 +1,305 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each test fixes the oracle to mathematics or an independent route: brute-force
+dense attention with an explicit -inf mask (numpy), torch's fp64
+scaled_dot_product_attention, closed forms, the Cauchy-Schwarz invariant, the
+shift invariance of softmax that the method relies on, exact special cases of
+the fp32 norm recipe, and the hand-counted workload sizes in tests/golden.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_video_row_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "workloads.json")
+
+
+def _f64(x):
+    return synth.bf16_bits_to_f64(x)
+
+
+def _rand_qkv(B, H, L, D, seed=7):
+    q = synth.tensor_bf16(seed, synth.TAG_Q, B, H, L, D)
+    k = synth.tensor_bf16(seed, synth.TAG_K, B, H, L, D)
+    v = synth.tensor_bf16(seed, synth.TAG_V, B, H, L, D)
+    return q, k, v
+
+
+def _brute_dense(q, k, v, mask, bs, scale):
+    """Dense route: full S = scale Q K^T over every key, element mask from the block mask."""
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    B, H, L, D = qf.shape
+    blk = np.arange(L) // bs
+    allowed = mask.astype(bool)[blk[:, None], blk[None, :]]  # [L, L]
+    O = np.zeros((B, H, L, D))
+    LSE = np.full((B, H, L), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            S = scale * (qf[b, h] @ kf[b, h].T)
+            S = np.where(allowed, S, -np.inf)
+            mu = S.max(axis=1, keepdims=True)
+            has = np.isfinite(mu[:, 0])
+            mu = np.where(np.isfinite(mu), mu, 0.0)
+            P = np.exp(S - mu)
+            l = P.sum(axis=1, keepdims=True)
+            O[b, h] = np.where(has[:, None], (P @ vf[b, h]) / np.where(l > 0, l, 1.0), 0.0)
+            LSE[b, h] = np.where(has, mu[:, 0] + np.log(np.where(l[:, 0] > 0, l[:, 0], 1.0)), -np.inf)
+    return O.reshape(-1, D), LSE.reshape(-1)
+
+
+# ------------------------------------------------------------------------------------------------
+# attention values
+
+
+@pytest.mark.parametrize("name", ["tiny"])
+def test_brute_force_dense_tiny(name):
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.make_qkv(w)
+    O, lse, _ = oracle.attention(q, k, v, w.block_mask(), w.block, w.scale)
+    Ob, lseb = _brute_dense(q, k, v, w.block_mask(), w.block, w.scale)
+    assert np.max(np.abs(O - Ob)) <= 1e-12
+    assert np.max(np.abs(lse - lseb)) <= 1e-12
+
+
+def test_brute_force_asymmetric_mask():
+    # first frame global is not symmetric: a transposed mask would fail here
+    B, H, D, nb, bs = 1, 2, 64, 8, 16
+    mask = synth.window_mask(nb, 2, True)
+    assert not np.array_equal(mask, mask.T)
+    q, k, v = _rand_qkv(B, H, nb * bs, D)
+    scale = float(np.float32(1 / 8))
+    O, lse, _ = oracle.attention(q, k, v, mask, bs, scale)
+    Ob, lseb = _brute_dense(q, k, v, mask, bs, scale)
+    assert np.max(np.abs(O - Ob)) <= 1e-12
+    assert np.max(np.abs(lse - lseb)) <= 1e-12
+    Ot, _, _ = oracle.attention(q, k, v, mask.T.copy(), bs, scale)
+    assert np.max(np.abs(Ot - Ob)) > 1e-3
+
+
+def test_random_masks_with_empty_rows():
+    rng = np.random.default_rng(3)
+    B, H, D, nb, bs = 2, 2, 64, 6, 16
+    q, k, v = _rand_qkv(B, H, nb * bs, D, seed=11)
+    for _ in range(3):
+        mask = (rng.random((nb, nb)) < 0.4).astype(np.uint8)
+        mask[2, :] = 0  # a query block that reads nothing
+        O, lse, l = oracle.attention(q, k, v, mask, bs, 0.125)
+        Ob, lseb = _brute_dense(q, k, v, mask, bs, 0.125)
+        assert np.max(np.abs(O - Ob)) <= 1e-12
+        fin = np.isfinite(lseb)
+        assert np.array_equal(fin, np.isfinite(lse))
+        assert np.max(np.abs(lse[fin] - lseb[fin])) <= 1e-12
+        # empty rows: O = 0, LSE = -inf, l = 0
+        rows = (np.arange(B * H * nb * bs) % (nb * bs)) // bs == 2
+        assert np.all(O[rows] == 0) and np.all(np.isneginf(lse[rows])) and np.all(l[rows] == 0)
+
+
+@pytest.mark.parametrize("dense", [True, False])
+def test_torch_sdpa_fp64(dense):
+    B, H, D, nb, bs = 1, 3, 128, 5, 32
+    L = nb * bs
+    q, k, v = _rand_qkv(B, H, L, D, seed=5)
+    mask = synth.dense_mask(nb) if dense else synth.window_mask(nb, 1, True)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    O, _, _ = oracle.attention(q, k, v, mask, bs, scale)
+    blk = torch.arange(L) // bs
+    m = torch.from_numpy(mask.astype(bool))[blk[:, None], blk[None, :]]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(_f64(q)), torch.from_numpy(_f64(k)), torch.from_numpy(_f64(v)),
+        attn_mask=m, scale=scale)
+    assert np.max(np.abs(O - ref.numpy().reshape(-1, D))) <= 1e-12
+
+
+def test_closed_forms():
+    B, H, D, nb, bs = 1, 2, 64, 4, 16
+    L = nb * bs
+    mask = synth.window_mask(nb, 1, True)
+    q, k, v = _rand_qkv(B, H, L, D, seed=9)
+    vf = _f64(v)
+    blk = np.arange(L) // bs
+    allowed = mask.astype(bool)[blk[:, None], blk[None, :]]
+
+    # q_i = 0: every allowed key gets weight 1/n -> mean of allowed v_j
+    qz = q.copy()
+    qz[0, 1, 20] = 0
+    O, _, _ = oracle.attention(qz, k, v, mask, bs, 0.125)
+    want = vf[0, 1][allowed[20]].mean(axis=0)
+    assert np.max(np.abs(O[L + 20] - want)) <= 1e-14
+
+    # all keys equal: the same mean for every row
+    ke = np.broadcast_to(k[:, :, :1, :], k.shape).copy()
+    O, _, _ = oracle.attention(q, ke, v, mask, bs, 0.125)
+    for i in (0, 17, 40, 63):
+        assert np.max(np.abs(O[i] - vf[0, 0][allowed[i]].mean(axis=0))) <= 1e-13
+
+    # constant values: O = c
+    c = synth.f32_to_bf16_bits(np.array([1.5], np.float32))[0]
+    vc = np.full_like(v, c)
+    O, _, _ = oracle.attention(q, k, vc, mask, bs, 0.125)
+    assert np.max(np.abs(O - 1.5)) <= 1e-14
+
+    # one dominant key: k_j = 64 * q_i (exact in bf16) -> O_i ~ v_j
+    kd = k.copy()
+    i, j = 37, 5  # row 37 is in block 2, which reads block 0 (global first frame)
+    assert allowed[i, j]
+    kd[0, 0, j] = synth.f32_to_bf16_bits(_f64(q[0, 0, i]).astype(np.float32) * 64)
+    O, _, _ = oracle.attention(q, kd, v, mask, bs, 0.125)
+    assert np.max(np.abs(O[i] - vf[0, 0, j])) <= 1e-6
+
+    # permuting keys (with their values) inside a block leaves O unchanged
+    perm = np.arange(L)
+    rng = np.random.default_rng(1)
+    for b0 in range(nb):
+        perm[b0 * bs:(b0 + 1) * bs] = b0 * bs + rng.permutation(bs)
+    O1, _, _ = oracle.attention(q, k, v, mask, bs, 0.125)
+    O2, _, _ = oracle.attention(q, k[:, :, perm], v[:, :, perm], mask, bs, 0.125)
+    assert np.max(np.abs(O1 - O2)) <= 1e-13
+
+
+def test_two_key_softmax():
+    # one token per block, two blocks, both read: S = (0, s) for query e_0
+    D = 16
+    one = synth.f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    q = np.zeros((1, 1, 2, D), np.uint16)
+    k = np.zeros_like(q)
+    v = np.zeros_like(q)
+    q[0, 0, 0, 0] = one
+    k[0, 0, 1, 0] = one              # k_0 = 0, k_1 = e_0
+    v[0, 0, 0, 1] = one              # v_0 = e_1, v_1 = 4 e_2
+    v[0, 0, 1, 2] = synth.f32_to_bf16_bits(np.array([4.0], np.float32))[0]
+    s = float(np.float32(math.log(3.0)))
+    O, lse, _ = oracle.attention(q, k, v, np.ones((2, 2), np.uint8), 1, s)
+    p1 = math.exp(s) / (1 + math.exp(s))
+    assert abs(O[0, 1] - (1 - p1)) <= 1e-15 and abs(O[0, 2] - 4 * p1) <= 1e-15
+    assert abs(lse[0] - math.log(1 + math.exp(s))) <= 1e-15
+
+
+# ------------------------------------------------------------------------------------------------
+# the bound
+
+
+def test_cauchy_schwarz_invariant_and_shift_invariance():
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = synth.make_qkv(w)
+    mask, bs, scale = w.block_mask(), w.block, w.scale
+    qn, kn = oracle.row_norms_f64(q), oracle.row_norms_f64(k)
+    M = oracle.row_bounds_f64(qn, kn, mask, bs, scale)
+    _, _, m32 = oracle.metadata_f32(q, k, mask, bs, scale)
+    qf, kf = _f64(q), _f64(k)
+    L = w.L
+    blk = np.arange(L) // bs
+    allowed = mask.astype(bool)[blk[:, None], blk[None, :]]
+    for b in range(w.B):
+        for h in range(w.H):
+            S = scale * (qf[b, h] @ kf[b, h].T)
+            S = np.where(allowed, S, -np.inf)
+            assert np.all(S <= M[b, h][:, None] * (1 + 1e-12))
+            assert np.all(S <= m32[b, h][:, None].astype(np.float64) * (1 + 2.0 ** -20))
+    # softmax with the bound as its shift equals softmax with the max shift
+    O_max, lse_max, _ = oracle.attention(q, k, v, mask, bs, scale)
+    O_cs, lse_cs, l_cs = oracle.attention(q, k, v, mask, bs, scale, shift=M.reshape(-1))
+    assert np.max(np.abs(O_cs - O_max)) <= 1e-12
+    assert np.max(np.abs(lse_cs - lse_max)) <= 1e-12
+    # l under the bound shift is exp(LSE - M) <= n_allowed
+    assert np.max(np.abs(np.log(l_cs) - (lse_max - M.reshape(-1)))) <= 1e-12
+
+
+def test_bound_shift_underflow_case_is_detectable():
+    # a key scaled to ~1e4 makes the bound far above every logit of rows that read it
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = synth.make_qkv(w)
+    k = k.copy()
+    big = _f64(k[0, 0, 3]) * 1.0e4
+    k[0, 0, 3] = synth.f32_to_bf16_bits(big.astype(np.float32))
+    mask, bs, scale = w.block_mask(), w.block, w.scale
+    _, lse, _ = oracle.attention(q, k, v, mask, bs, scale)
+    _, _, m32 = oracle.metadata_f32(q, k, mask, bs, scale)
+    gap = m32.reshape(-1).astype(np.float64) - lse       # -ln(l under the bound shift)
+    reads0 = (np.arange(w.B * w.H * w.L) // w.L == 0) & ((np.arange(w.B * w.H * w.L) % w.L) // bs <= 1)
+    assert np.all(gap[reads0] > 100.0)                   # flagged: l < 2^-64
+    assert np.all(gap[~reads0] < 30.0)                   # untouched rows keep l >> 2^-64
+
+
+# ------------------------------------------------------------------------------------------------
+# the fp32 norm recipe
+
+
+def _bits(vals, D):
+    x = np.zeros((1, D), np.float32)
+    for i, val in vals:
+        x[0, i] = val
+    return synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("D", [16, 64, 128])
+def test_norm_recipe_exact_cases(D):
+    assert oracle.row_norms_f32(_bits([], D))[0] == 0.0
+    ones = synth.f32_to_bf16_bits(np.ones((1, D), np.float32))
+    assert oracle.row_norms_f32(ones)[0] == np.sqrt(np.float32(D))
+    for x in (3.0, -0.75, 2.0 ** 60, 2.0 ** -70):
+        assert oracle.row_norms_f32(_bits([(D // 2 + 1, x)], D))[0] == np.float32(abs(x))
+    assert np.isinf(oracle.row_norms_f32(_bits([(0, 2.0 ** 64)], D))[0])
+
+
+@pytest.mark.parametrize("D,w_exact", [(16, 2 ** 24 + 14), (64, 2 ** 24 + 60), (128, 2 ** 24 + 120)])
+def test_norm_recipe_order(D, w_exact):
+    # x_0 = 4096 and every other element 1: within chunk 0 each +1 is lost (ties to even at 2^24);
+    # the other 15 chunks hold (D/16) each and meet chunk 0 through the 8-4-2-1 tree, which keeps them.
+    # Hand count: D=16 -> 2^24 + 14, D=64 -> 2^24 + 60, D=128 -> 2^24 + 120 (a plain sequential sum
+    # would stay at 2^24, the exact sum is 2^24 + D - 1).
+    x = np.ones((1, D), np.float32)
+    x[0, 0] = 4096.0
+    n = oracle.row_norms_f32(synth.f32_to_bf16_bits(x))[0]
+    assert n == np.sqrt(np.float32(w_exact))
+    assert n != np.sqrt(np.float32(2 ** 24))
+
+
+def test_norm_recipe_vs_fp64_and_bounds():
+    w = synth.WORKLOADS["small"]
+    q, k, _ = synth.make_qkv(w)
+    mask, bs, scale = w.block_mask(), w.block, w.scale
+    qn32, km32, rb32 = oracle.metadata_f32(q, k, mask, bs, scale)
+    qn64, kn64 = oracle.row_norms_f64(q), oracle.row_norms_f64(k)
+    assert np.max(np.abs(qn32 / qn64 - 1)) <= 2.0 ** -20
+    km64 = kn64.reshape(w.B, w.H, w.nb, bs).max(axis=-1)
+    assert np.max(np.abs(km32 / km64 - 1)) <= 2.0 ** -20
+    M = oracle.row_bounds_f64(qn64, kn64, mask, bs, scale)
+    assert np.max(np.abs(rb32 / M - 1)) <= 2.0 ** -20
+    # kmax is a max of norms: exact, and equal to one of them
+    kn32 = oracle.row_norms_f32(k).reshape(w.B, w.H, w.nb, bs)
+    assert np.array_equal(km32, kn32.max(axis=-1))
+
+
+# ------------------------------------------------------------------------------------------------
+# workload sizes and the allowed-block sets
+
+
+def test_workload_sizes_golden():
+    g = json.load(open(GOLDEN))["workloads"]
+    for name, w in synth.WORKLOADS.items():
+        row_ptr, col_idx = oracle.allowed_csr(w.block_mask())
+        assert len(col_idx) == g[name]["nnz"], name
+        assert (w.B, w.H, w.D, w.frames, w.block) == (g[name]["B"], g[name]["H"], g[name]["D"],
+                                                       g[name]["frames"], g[name]["block"])
+        assert synth.useful_flop(w) == g[name]["useful_flop"]
+        # ascending within each query block
+        for qb in range(w.nb):
+            s = col_idx[row_ptr[qb]:row_ptr[qb + 1]]
+            assert np.all(np.diff(s) > 0)
+
+
+def test_generator_matches_splitmix64_definition():
+    # published SplitMix64 outputs for state 1234567
+    assert [synth.splitmix64_at(1234567, i) for i in range(3)] == [
+        6457827717110365317, 3203168211198807973, 9817491932198370423]
+    # fp32 -> bf16 round-to-nearest-even on ties
+    x = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -7], np.float32)
+    assert list(synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(x))) == [1.0, 1 + 2 ** -6, 1 + 2 ** -7]
+    q = _f64(synth.tensor_bf16(0, synth.TAG_Q, 1, 2, 4096, 64))
+    assert abs(q.mean()) < 0.01 and abs(q.std() - 1) < 0.01
