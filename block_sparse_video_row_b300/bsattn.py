@@ -1,0 +1,237 @@
+"""Python binding of libbsattn.so (the C ABI in include/bsattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  The functions keep the C names (``bsattn_create_layout``,
+``bsattn_row_bounds``, ``bsattn_forward``, ``bsattn_destroy``, ...).  Tensors
+may be ``torch.Tensor`` (their ``data_ptr()`` is passed) or raw integer device
+pointers; streams may be ``torch.cuda.Stream`` or raw ``cudaStream_t`` ints.
+PyTorch is used only for device memory and streams.
+
+There is no fallback: if the compiled library is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsattn.so")
+
+BSATTN_OK = 0
+BSATTN_ERR_INVALID_ARG = 1
+BSATTN_ERR_UNALIGNED_BLOCK = 2
+BSATTN_ERR_UNSUPPORTED = 3
+BSATTN_ERR_CUDA = 4
+BSATTN_ERR_OOM = 5
+BSATTN_ERR_TIMEOUT = 6
+BSATTN_ERR_DEVICE = 7
+
+BSATTN_BOUND = 0
+BSATTN_ONLINE_MAX = 1
+BSATTN_NO_FALLBACK = 2
+BSATTN_PLAN_ONLY = 0x10
+
+EXPORTED = ("bsattn_create_layout", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
+            "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export")
+
+
+class LayoutInfo(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("nb", ctypes.c_int32), ("L", ctypes.c_int64),
+                ("nnz_blocks", ctypes.c_int32), ("kv_tile", ctypes.c_int32),
+                ("q_tiles_per_block", ctypes.c_int32), ("n_units", ctypes.c_int32),
+                ("mma_rows", ctypes.c_int64), ("useful_flop", ctypes.c_double)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class BsattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load (once) and return the ctypes handle of libbsattn.so."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libbsattn.so not built ({p}); run block_sparse_video_row_b300._build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.bsattn_create_layout.restype = i32
+    lib.bsattn_create_layout.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i32, i32, vp, i32]
+    lib.bsattn_row_bounds.restype = i32
+    lib.bsattn_row_bounds.argtypes = [vp, vp, vp, f32, vp, vp, vp, vp]
+    lib.bsattn_forward.restype = i32
+    lib.bsattn_forward.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i32, vp]
+    lib.bsattn_destroy.restype = None
+    lib.bsattn_destroy.argtypes = [vp]
+    lib.bsattn_status_string.restype = ctypes.c_char_p
+    lib.bsattn_status_string.argtypes = [i32]
+    lib.bsattn_query_stats.restype = i32
+    lib.bsattn_query_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i32), vp]
+    lib.bsattn_layout_info.restype = i32
+    lib.bsattn_layout_info.argtypes = [vp, ctypes.POINTER(LayoutInfo)]
+    lib.bsattn_layout_export.restype = i32
+    lib.bsattn_layout_export.argtypes = [vp, vp, vp, vp]
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    if isinstance(x, np.ndarray):
+        return int(x.ctypes.data)
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except Exception:
+            pass
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def status_string(status: int) -> str:
+    return load().bsattn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != BSATTN_OK:
+        raise BsattnError(status, what)
+
+
+class Layout:
+    """Owns a bsattn_layout_t; freed by destroy() or when garbage collected."""
+
+    def __init__(self, handle: int, mask: np.ndarray):
+        self.handle = handle
+        self.mask = mask
+        self.info = bsattn_layout_info(self)
+
+    def destroy(self):
+        if self.handle:
+            load().bsattn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.destroy()
+
+
+def bsattn_create_layout(B: int, H: int, L: int, D: int, block_size: int, block_mask, flags: int = 0,
+                         raise_on_error: bool = True):
+    """Returns a Layout (or, with raise_on_error=False, the pair (status, Layout or None))."""
+    m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
+    h = ctypes.c_void_p()
+    st = load().bsattn_create_layout(ctypes.byref(h), B, H, L, D, block_size, m.ctypes.data, flags)
+    if not raise_on_error:
+        return st, (Layout(h.value, m) if st == BSATTN_OK else None)
+    _check(st, "bsattn_create_layout")
+    return Layout(h.value, m)
+
+
+def bsattn_row_bounds(lay: Layout, q, k, scale: float, qnorm, kmax, rowbound, stream=None,
+                      raise_on_error: bool = True) -> int:
+    st = load().bsattn_row_bounds(lay.handle, _ptr(q), _ptr(k), float(scale), _ptr(qnorm), _ptr(kmax),
+                                  _ptr(rowbound), _stream(stream))
+    if raise_on_error:
+        _check(st, "bsattn_row_bounds")
+    return st
+
+
+def bsattn_forward(lay: Layout, q, k, v, o, scale: float, rowbound, lse=None, flags: int = 0, stream=None,
+                   raise_on_error: bool = True) -> int:
+    st = load().bsattn_forward(lay.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), float(scale), _ptr(rowbound),
+                               _ptr(lse), flags, _stream(stream))
+    if raise_on_error:
+        _check(st, "bsattn_forward")
+    return st
+
+
+def bsattn_destroy(lay: Layout) -> None:
+    lay.destroy()
+
+
+def bsattn_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def bsattn_query_stats(lay: Layout, stream=None):
+    """(fallback_rows, fallback_units, device_status); synchronises the stream."""
+    rows, units, dev = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    _check(load().bsattn_query_stats(lay.handle, ctypes.byref(rows), ctypes.byref(units), ctypes.byref(dev),
+                                     _stream(stream)), "bsattn_query_stats")
+    return rows.value, units.value, dev.value
+
+
+def bsattn_layout_info(lay: Layout) -> LayoutInfo:
+    info = LayoutInfo()
+    _check(load().bsattn_layout_info(lay.handle, ctypes.byref(info)), "bsattn_layout_info")
+    return info
+
+
+def bsattn_layout_export(lay: Layout):
+    """(row_ptr [nb+1], col_idx [nnz], units [n_units, 4]) as int32 numpy arrays."""
+    i = lay.info
+    row_ptr = np.zeros(i.nb + 1, np.int32)
+    col_idx = np.zeros(max(i.nnz_blocks, 1), np.int32)
+    units = np.zeros((i.n_units, 4), np.int32)
+    _check(load().bsattn_layout_export(lay.handle, row_ptr.ctypes.data, col_idx.ctypes.data, units.ctypes.data),
+           "bsattn_layout_export")
+    return row_ptr, col_idx[:i.nnz_blocks].copy(), units
+
+
+# ------------------------------------------------------------------------------------------------
+# convenience: one call for bounds + forward on torch tensors
+
+
+def attention(q, k, v, block_mask, block_size: int, scale: Optional[float] = None, flags: int = 0,
+              return_lse: bool = False, layout: Optional[Layout] = None, stream=None):
+    """O = block-sparse attention of bf16 [B,H,L,D] CUDA tensors (allocates O, metadata and LSE with torch)."""
+    import torch
+    B, H, L, D = q.shape
+    if scale is None:
+        scale = float(np.float32(1.0 / np.sqrt(D)))
+    lay = layout or bsattn_create_layout(B, H, L, D, block_size, block_mask)
+    nb = L // block_size
+    dev = q.device
+    o = torch.empty_like(q)
+    qnorm = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    kmax = torch.empty((B, H, nb), dtype=torch.float32, device=dev)
+    rowbound = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev) if return_lse else None
+    if not (flags & BSATTN_ONLINE_MAX):
+        bsattn_row_bounds(lay, q, k, scale, qnorm, kmax, rowbound, stream)
+    bsattn_forward(lay, q, k, v, o, scale, rowbound, lse, flags, stream)
+    return (o, lse) if return_lse else o

@@ -1,0 +1,399 @@
+// The C ABI of libbsattn.so: argument checks, the host plan (allowed key blocks,
+// key tile, work list), device buffers, TMA tensor maps and kernel launches.
+// The operation and its conventions are documented in include/bsattn.h.
+#include "bsattn.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+struct bsattn_layout_s {
+    int32_t B = 0, H = 0, D = 0, bs = 0, nb = 0;
+    int64_t L = 0;
+    bool plan_only = false;
+    std::vector<int32_t> row_ptr, col_idx, units;
+    int32_t kv_tile = 0, qt_per_block = 0, n_units = 0;
+    int64_t mma_rows = 0;
+    double useful_flop = 0.0;
+    int device = -1, num_sms = 0;
+    int32_t *d_row_ptr = nullptr, *d_col_idx = nullptr;
+    int4 *d_units = nullptr;
+    int32_t *d_ws = nullptr;
+    bsv::Workspace ws{};
+    uint64_t timeout_ns = 0;
+};
+
+namespace {
+
+constexpr int kWsHeader = 8;  // int32 slots: [0] status, [4] fb_count, [5] fb_rows
+
+bsattn_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return BSATTN_OK;
+    return e == cudaErrorMemoryAllocation ? BSATTN_ERR_OOM : BSATTN_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Key tile: the largest multiple of 16 that divides the frame block, at most 128
+// (a tile must never straddle a frame edge: no element mask on the key side).
+int32_t choose_kv_tile(int32_t bs) {
+    for (int32_t n = bsv::kMaxKvTile; n >= 16; n -= 16)
+        if (bs % n == 0) return n;
+    return 16;
+}
+
+void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
+    const int32_t nb = lay.nb;
+    lay.row_ptr.assign(static_cast<size_t>(nb) + 1, 0);
+    lay.col_idx.clear();
+    for (int32_t qb = 0; qb < nb; ++qb) {
+        for (int32_t kb = 0; kb < nb; ++kb)
+            if (mask[static_cast<int64_t>(qb) * nb + kb]) lay.col_idx.push_back(kb);
+        lay.row_ptr[qb + 1] = static_cast<int32_t>(lay.col_idx.size());
+    }
+    lay.kv_tile = choose_kv_tile(lay.bs);
+    lay.qt_per_block = (lay.bs + bsv::kQTile - 1) / bsv::kQTile;
+    const int32_t tpb = lay.bs / lay.kv_tile;
+
+    struct Unit {
+        int32_t bh, qb, qt0, nt;
+        int64_t cost;
+    };
+    std::vector<Unit> us;
+    const int32_t BH = lay.B * lay.H;
+    us.reserve(static_cast<size_t>(BH) * nb * ((lay.qt_per_block + 1) / 2));
+    for (int32_t bh = 0; bh < BH; ++bh)
+        for (int32_t qb = 0; qb < nb; ++qb) {
+            const int64_t nkv = static_cast<int64_t>(lay.row_ptr[qb + 1] - lay.row_ptr[qb]) * tpb;
+            for (int32_t qt0 = 0; qt0 < lay.qt_per_block; qt0 += 2) {
+                const int32_t nt = std::min(2, lay.qt_per_block - qt0);
+                us.push_back({bh, qb, qt0, nt, nkv * nt});
+            }
+        }
+    // Largest first (longest-processing-time order for the persistent CTAs); equal
+    // costs keep (head, frame, tile) order so concurrently running CTAs share K/V in L2.
+    std::stable_sort(us.begin(), us.end(), [](const Unit &a, const Unit &b) { return a.cost > b.cost; });
+    lay.n_units = static_cast<int32_t>(us.size());
+    lay.units.resize(us.size() * 4);
+    for (size_t i = 0; i < us.size(); ++i) {
+        lay.units[4 * i + 0] = us[i].bh;
+        lay.units[4 * i + 1] = us[i].qb;
+        lay.units[4 * i + 2] = us[i].qt0;
+        lay.units[4 * i + 3] = us[i].nt;
+    }
+    int64_t reading_frames = 0;
+    for (int32_t qb = 0; qb < nb; ++qb) reading_frames += lay.row_ptr[qb + 1] > lay.row_ptr[qb] ? 1 : 0;
+    lay.mma_rows = static_cast<int64_t>(BH) * reading_frames * lay.qt_per_block * bsv::kQTile;
+    lay.useful_flop = 4.0 * static_cast<double>(lay.col_idx.size()) * static_cast<double>(lay.bs) *
+                      static_cast<double>(lay.bs) * lay.D * lay.H * lay.B;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once (no link-time libcuda dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Q (and O) viewed as [B*H*nb frames][block rows][D]: a 128-row box that starts
+// inside a frame and runs past its end reads zeros there (never the next frame).
+bool encode_q_map(CUtensorMap *m, const bsattn_layout_s &lay, const void *ptr) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(lay.D), static_cast<cuuint64_t>(lay.bs),
+                                static_cast<cuuint64_t>(lay.B) * lay.H * lay.nb};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lay.D) * 2,
+                                   static_cast<cuuint64_t>(lay.D) * 2 * lay.bs};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bsv::kQTile), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K and V viewed as [B*H*L rows][D]; boxes of kv_tile rows never leave a frame.
+bool encode_kv_map(CUtensorMap *m, const bsattn_layout_s &lay, const void *ptr) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lay.D),
+                                static_cast<cuuint64_t>(lay.B) * lay.H * static_cast<cuuint64_t>(lay.L)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lay.D) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(lay.kv_tile)};
+    const cuuint32_t es[2] = {1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void free_device(bsattn_layout_s *lay) {
+    if (lay->d_row_ptr) cudaFree(lay->d_row_ptr);
+    if (lay->d_col_idx) cudaFree(lay->d_col_idx);
+    if (lay->d_units) cudaFree(lay->d_units);
+    if (lay->d_ws) cudaFree(lay->d_ws);
+    lay->d_row_ptr = lay->d_col_idx = nullptr;
+    lay->d_units = nullptr;
+    lay->d_ws = nullptr;
+}
+
+bsattn_status setup_device(bsattn_layout_s &lay) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BSATTN_ERR_DEVICE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BSATTN_ERR_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return BSATTN_ERR_DEVICE;  // built for sm_103a only
+    if (!encode_fn()) return BSATTN_ERR_CUDA;
+    lay.device = dev;
+    lay.num_sms = prop.multiProcessorCount;
+
+    cudaError_t e = lay.D == 128 ? bsv::configure_attention_d128(lay.kv_tile)
+                                 : bsv::configure_attention_d64(lay.kv_tile);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    const size_t nnz = std::max<size_t>(lay.col_idx.size(), 1);
+    const size_t ws_ints = kWsHeader + 2 * static_cast<size_t>(lay.n_units);
+    if ((e = cudaMalloc(&lay.d_row_ptr, lay.row_ptr.size() * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&lay.d_col_idx, nnz * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&lay.d_units, static_cast<size_t>(lay.n_units) * sizeof(int4))) != cudaSuccess ||
+        (e = cudaMalloc(&lay.d_ws, ws_ints * 4)) != cudaSuccess) {
+        free_device(&lay);
+        return from_cuda(e);
+    }
+    if ((e = cudaMemcpy(lay.d_row_ptr, lay.row_ptr.data(), lay.row_ptr.size() * 4, cudaMemcpyHostToDevice)) !=
+            cudaSuccess ||
+        (!lay.col_idx.empty() &&
+         (e = cudaMemcpy(lay.d_col_idx, lay.col_idx.data(), lay.col_idx.size() * 4, cudaMemcpyHostToDevice)) !=
+             cudaSuccess) ||
+        (e = cudaMemcpy(lay.d_units, lay.units.data(), lay.units.size() * 4, cudaMemcpyHostToDevice)) !=
+            cudaSuccess ||
+        (e = cudaMemset(lay.d_ws, 0, ws_ints * 4)) != cudaSuccess) {
+        free_device(&lay);
+        return from_cuda(e);
+    }
+    lay.ws.status = lay.d_ws + 0;
+    lay.ws.fb_count = lay.d_ws + 4;
+    lay.ws.fb_rows = lay.d_ws + 5;
+    lay.ws.unit_flag = lay.d_ws + kWsHeader;
+    lay.ws.fb_list = lay.d_ws + kWsHeader + lay.n_units;
+
+    uint64_t ms = 4000;
+    if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
+        const long long v = std::atoll(env);
+        if (v > 0) ms = static_cast<uint64_t>(v);
+    }
+    lay.timeout_ns = ms * 1000000ull;
+    return BSATTN_OK;
+}
+
+bsattn_status check_runnable(const bsattn_layout_s *lay) {
+    if (!lay || lay->plan_only) return BSATTN_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != lay->device) return BSATTN_ERR_INVALID_ARG;
+    return BSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,
+                                   int32_t block_size, const uint8_t *block_mask, int32_t flags) {
+    if (!out) return BSATTN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!block_mask || B < 1 || H < 1 || L < 1 || block_size < 1) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~BSATTN_PLAN_ONLY) != 0) return BSATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+    if (block_size % 16 != 0 || L % block_size != 0) return BSATTN_ERR_UNALIGNED_BLOCK;
+    const int64_t nb = L / block_size;
+    if (nb > BSATTN_MAX_NB) return BSATTN_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(B) * H * L > BSATTN_MAX_ROWS) return BSATTN_ERR_UNSUPPORTED;
+
+    bsattn_layout_s *lay = new (std::nothrow) bsattn_layout_s;
+    if (!lay) return BSATTN_ERR_OOM;
+    try {
+        lay->B = B;
+        lay->H = H;
+        lay->L = L;
+        lay->D = D;
+        lay->bs = block_size;
+        lay->nb = static_cast<int32_t>(nb);
+        lay->plan_only = (flags & BSATTN_PLAN_ONLY) != 0;
+        build_plan(*lay, block_mask);
+    } catch (const std::bad_alloc &) {
+        delete lay;
+        return BSATTN_ERR_OOM;
+    }
+    if (!lay->plan_only) {
+        const bsattn_status st = setup_device(*lay);
+        if (st != BSATTN_OK) {
+            delete lay;
+            return st;
+        }
+    }
+    *out = lay;
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *k, float scale, float *qnorm,
+                                float *kmax, float *rowbound, bsattn_stream_t stream) {
+    bsattn_status st = check_runnable(lay);
+    if (st != BSATTN_OK) return st;
+    if (!q || !k || !qnorm || !kmax || !rowbound) return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(qnorm) & 3) ||
+        (reinterpret_cast<uintptr_t>(kmax) & 3) || (reinterpret_cast<uintptr_t>(rowbound) & 3))
+        return BSATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bsv::BoundsParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k);
+    p.qnorm = qnorm;
+    p.kmax_bits = reinterpret_cast<uint32_t *>(kmax);
+    p.rowbound = rowbound;
+    p.row_ptr = lay->d_row_ptr;
+    p.col_idx = lay->d_col_idx;
+    p.L = lay->L;
+    p.block = lay->bs;
+    p.nb = lay->nb;
+    p.BH = lay->B * lay->H;
+    p.chunks_per_block = (lay->bs + bsv::bounds_chunk_rows() - 1) / bsv::bounds_chunk_rows();
+    p.scale = scale;
+    cudaError_t e = cudaMemsetAsync(kmax, 0, static_cast<size_t>(p.BH) * lay->nb * 4, s);
+    if (e == cudaSuccess) e = bsv::launch_norms(p, lay->D, s);
+    if (e == cudaSuccess) e = bsv::launch_rowbound(p, s);
+    return from_cuda(e);
+}
+
+bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, const void *v, void *o,
+                             float scale, const float *rowbound, float *lse, int32_t flags,
+                             bsattn_stream_t stream) {
+    bsattn_status st = check_runnable(lay);
+    if (st != BSATTN_OK) return st;
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK)) != 0) return BSATTN_ERR_INVALID_ARG;
+    const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
+    if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BSATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(rowbound) & 3) || (reinterpret_cast<uintptr_t>(lse) & 3))
+        return BSATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_q_map(&tq, *lay, q) || !encode_kv_map(&tk, *lay, k) || !encode_kv_map(&tv, *lay, v))
+        return BSATTN_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // per-call part of the workspace: fb_count, fb_rows and the unit flags
+    cudaError_t e = cudaMemsetAsync(lay->d_ws + 4, 0, (kWsHeader - 4 + static_cast<size_t>(lay->n_units)) * 4, s);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    bsv::AttnParams p;
+    p.units = lay->d_units;
+    p.n_units = lay->n_units;
+    p.row_ptr = lay->d_row_ptr;
+    p.col_idx = lay->d_col_idx;
+    p.rowbound = rowbound;
+    p.o = static_cast<uint16_t *>(o);
+    p.lse = lse;
+    p.ws = lay->ws;
+    p.L = lay->L;
+    p.block = lay->bs;
+    p.nb = lay->nb;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.timeout_ns = lay->timeout_ns;
+    const int grid = std::max(1, std::min(lay->n_units, lay->num_sms));
+    auto launch = [&](bool on) {
+        return lay->D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, lay->kv_tile, on, grid, s)
+                             : bsv::launch_attention_d64(tq, tk, tv, p, lay->kv_tile, on, grid, s);
+    };
+    if (online) {
+        p.mode = bsv::kModeOnlineAll;
+        return from_cuda(launch(true));
+    }
+    p.mode = bsv::kModeBound;
+    e = launch(false);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (flags & BSATTN_NO_FALLBACK) return BSATTN_OK;
+    p.mode = bsv::kModeFallback;
+    return from_cuda(launch(true));
+}
+
+void bsattn_destroy(bsattn_layout_t lay) {
+    if (!lay) return;
+    if (!lay->plan_only) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (cur != lay->device) cudaSetDevice(lay->device);
+        free_device(lay);
+        if (cur != lay->device && cur >= 0) cudaSetDevice(cur);
+    }
+    delete lay;
+}
+
+const char *bsattn_status_string(bsattn_status st) {
+    switch (st) {
+        case BSATTN_OK: return "ok";
+        case BSATTN_ERR_INVALID_ARG: return "invalid argument";
+        case BSATTN_ERR_UNALIGNED_BLOCK: return "block size not a multiple of 16, or L not a multiple of it";
+        case BSATTN_ERR_UNSUPPORTED: return "unsupported size or head dim";
+        case BSATTN_ERR_CUDA: return "CUDA error";
+        case BSATTN_ERR_OOM: return "out of device memory";
+        case BSATTN_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case BSATTN_ERR_DEVICE: return "no usable sm_103 device";
+    }
+    return "unknown status";
+}
+
+bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, int64_t *fallback_units,
+                                 int32_t *device_status, bsattn_stream_t stream) {
+    bsattn_status st = check_runnable(lay);
+    if (st != BSATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    int32_t h[kWsHeader];
+    e = cudaMemcpy(h, lay->d_ws, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (fallback_units) *fallback_units = h[4];
+    if (fallback_rows) *fallback_rows = h[5];
+    if (device_status) *device_status = (h[0] & bsv::kStatusTimeout) ? BSATTN_ERR_TIMEOUT : BSATTN_OK;
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info) {
+    if (!lay || !info) return BSATTN_ERR_INVALID_ARG;
+    info->B = lay->B;
+    info->H = lay->H;
+    info->D = lay->D;
+    info->block_size = lay->bs;
+    info->nb = lay->nb;
+    info->L = lay->L;
+    info->nnz_blocks = static_cast<int32_t>(lay->col_idx.size());
+    info->kv_tile = lay->kv_tile;
+    info->q_tiles_per_block = lay->qt_per_block;
+    info->n_units = lay->n_units;
+    info->mma_rows = lay->mma_rows;
+    info->useful_flop = lay->useful_flop;
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units) {
+    if (!lay) return BSATTN_ERR_INVALID_ARG;
+    if (row_ptr) std::memcpy(row_ptr, lay->row_ptr.data(), lay->row_ptr.size() * 4);
+    if (col_idx && !lay->col_idx.empty()) std::memcpy(col_idx, lay->col_idx.data(), lay->col_idx.size() * 4);
+    if (units && !lay->units.empty()) std::memcpy(units, lay->units.data(), lay->units.size() * 4);
+    return BSATTN_OK;
+}
+
+}  // extern "C"

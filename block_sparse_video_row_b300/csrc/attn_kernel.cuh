@@ -1,0 +1,526 @@
+// Frame-aligned block-sparse attention forward on sm_103a: a persistent,
+// warp-specialised kernel with TMA-fed tcgen05 MMAs accumulating in TMEM.
+//
+// The method ("HeyGen Avatar IV on Trillium TPU" deep-dive, sections
+// 把 block 縮到 16 and 拿掉 softmax 的序列相依; "How is HeyGen optimizing AI video
+// on Google Cloud TPUs", section "Innovating Beyond Serial Dependencies"):
+//   * query and key blocks are whole frames; the mask says which key frames a
+//     query frame reads.  Key tiles are N keys with N a multiple of 16 that
+//     divides the frame, so a tile never crosses a frame edge and no element
+//     mask, tail pass or padding exists on the key side;
+//   * the softmax shift of row i is its Cauchy-Schwarz bound m_i (precomputed),
+//     so P = exp(scale*S - m_i) needs no running max and no rescaling of the
+//     accumulator: every key tile is independent.
+//
+// One CTA per SM processes work units: a unit is one or two 128-row query tiles
+// of the same frame (they share every K/V tile), looping over the unit's
+// allowed key tiles.
+//   warp 0     TMA producer: Q tiles, then a K ring and a V ring of STAGES tiles.
+//   warp 1     MMA issuer (one thread): S_t = Q_t K^T (A, B from smem) and
+//              O_t += P_t V (A = P_t from TMEM, B = V from smem), t = 0, 1.
+//   warps 4-7  softmax of query tile 0; warps 8-11 of tile 1 (one row per thread).
+// TMEM (512 columns): S_0/P_0 at column 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
+// P_t (bf16, two per 32-bit column) overwrites the first N/2 columns of S_t.
+//
+// Per key tile the MMA thread issues, in order, PV_0(j), S_0(j+1), PV_1(j),
+// S_1(j+1): while softmax 0 works on S_0 the tensor cores run tile 1's MMAs and
+// vice versa.  tcgen05 MMAs from one thread complete in issue order, so the
+// commit that signals S_t(j+1) also guarantees PV_t(j) has finished: O_t is
+// stable whenever its softmax holds S_t (the online variant rescales it then).
+//
+// Every mbarrier wait is bounded (a wall-clock limit); on expiry the CTA raises
+// a shared abort flag and a device status bit, lets in-flight copies and MMAs
+// land, frees its TMEM and returns.
+#pragma once
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsv {
+
+template <int D, int N>
+struct AttnCfg {
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(N % 16 == 0 && N >= 16 && N <= kMaxKvTile, "key tile");
+    static constexpr int DH = D / 64;                 // 64-column (128-byte) halves of a row
+    static constexpr int HALF_Q = kQTile * 128;       // bytes of one half of a Q tile
+    static constexpr int Q_TILE = DH * HALF_Q;
+    static constexpr int HALF_KV = N * 128;
+    static constexpr int KV_TILE = DH * HALF_KV;
+    static constexpr int SMEM_CAP = 232448;           // 227 KB per CTA
+    static constexpr int RESERVED = 2048;             // alignment slack + barrier block
+    static constexpr int STAGES_FIT = (SMEM_CAP - RESERVED - 2 * Q_TILE) / (2 * KV_TILE);
+    static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+    static_assert(STAGES >= 2, "shared memory");
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = 2 * Q_TILE;
+    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+    static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
+    static constexpr int SMEM_USED = OFF_BAR + RESERVED;
+    // Above half of the SM's shared memory, so one CTA (and one TMEM owner) per SM.
+    static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
+    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kQTile, N, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kQTile, D, false, true);
+};
+
+// Barrier block layout (uint64 slots).
+struct Bars {
+    uint64_t *q_full, *q_empty, *s_full, *p_full, *o_full, *k_full, *k_empty, *v_full, *v_empty, *drain;
+    uint32_t *tmem_slot;
+    volatile int *abort;
+};
+
+template <int STAGES>
+__device__ __forceinline__ Bars carve_bars(uint8_t *base) {
+    uint64_t *b = reinterpret_cast<uint64_t *>(base);
+    Bars r;
+    r.q_full = b + 0;
+    r.q_empty = b + 2;
+    r.s_full = b + 4;
+    r.p_full = b + 6;
+    r.o_full = b + 8;
+    r.drain = b + 10;
+    r.k_full = b + 12;
+    r.k_empty = r.k_full + STAGES;
+    r.v_full = r.k_empty + STAGES;
+    r.v_empty = r.v_full + STAGES;
+    r.tmem_slot = reinterpret_cast<uint32_t *>(r.v_empty + STAGES);
+    r.abort = reinterpret_cast<volatile int *>(r.tmem_slot + 1);
+    return r;
+}
+
+__device__ __forceinline__ int unit_index(const AttnParams &p, int i) {
+    return p.mode == kModeFallback ? p.ws.fb_list[i] : i;
+}
+
+// Wait that ignores the abort flag: used only to let already-issued copies/MMAs land.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) break;
+    }
+}
+
+// ----------------------------------------------------------------------------------------------
+// softmax of one S tile (one row per thread), P written back to TMEM as bf16
+
+// Bound softmax: P = 2^(S*c1 - m2), c1 = scale*log2(e), m2 = m_i*log2(e).
+template <int N>
+__device__ __forceinline__ void softmax_tile_bound(uint32_t tS, float c1, float m2, float &l0, float &l1) {
+    constexpr int NC = N / 16;
+#pragma unroll
+    for (int c = 0; c < NC; c += 2) {
+        uint32_t a[16], b[16];
+        tmem_ld16(tS + c * 16, a);
+        if (c + 1 < NC) tmem_ld16(tS + (c + 1) * 16, b);
+        tmem_wait_ld();
+        reg_fence16(a);
+        if (c + 1 < NC) reg_fence16(b);
+        uint32_t pa[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float x0 = ex2_approx(fmaf(__uint_as_float(a[2 * e]), c1, -m2));
+            const float x1 = ex2_approx(fmaf(__uint_as_float(a[2 * e + 1]), c1, -m2));
+            pa[e] = pack_bf16x2(x0, x1);
+            l0 += bf16lo_f32(pa[e]);
+            l1 += bf16hi_f32(pa[e]);
+        }
+        tmem_st8(tS + c * 8, pa);
+        if (c + 1 < NC) {
+            uint32_t pb[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float x0 = ex2_approx(fmaf(__uint_as_float(b[2 * e]), c1, -m2));
+                const float x1 = ex2_approx(fmaf(__uint_as_float(b[2 * e + 1]), c1, -m2));
+                pb[e] = pack_bf16x2(x0, x1);
+                l0 += bf16lo_f32(pb[e]);
+                l1 += bf16hi_f32(pb[e]);
+            }
+            tmem_st8(tS + (c + 1) * 8, pb);
+        }
+    }
+}
+
+template <int N>
+__device__ __forceinline__ float tile_row_max(uint32_t tS) {
+    constexpr int NC = N / 16;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < NC; c += 2) {
+        uint32_t a[16], b[16];
+        tmem_ld16(tS + c * 16, a);
+        if (c + 1 < NC) tmem_ld16(tS + (c + 1) * 16, b);
+        tmem_wait_ld();
+        reg_fence16(a);
+        if (c + 1 < NC) reg_fence16(b);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
+        if (c + 1 < NC) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(b[e]));
+        }
+    }
+    return mx;
+}
+
+// Multiply one row of the O accumulator (D fp32 columns) by alpha (warp-collective).
+template <int D>
+__device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        uint32_t a[16];
+        tmem_ld16(tO + c * 16, a);
+        tmem_wait_ld();
+        reg_fence16(a);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) * alpha);
+        tmem_st16(tO + c * 16, a);
+    }
+    tmem_wait_st();
+}
+
+// ----------------------------------------------------------------------------------------------
+
+template <int D, int N, bool ONLINE>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    using C = AttnCfg<D, N>;
+    const int n_seq = p.mode == kModeFallback ? *reinterpret_cast<volatile int32_t *>(p.ws.fb_count) : p.n_units;
+    if (static_cast<int>(blockIdx.x) >= n_seq) return;  // nothing to do: exit before any TMEM allocation
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars bar = carve_bars<C::STAGES>(smem + C::OFF_BAR);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tpb = p.block / N;  // key tiles per frame block
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar.q_full + t, 1);
+            mbar_init(bar.q_empty + t, 1);
+            mbar_init(bar.s_full + t, 1);
+            mbar_init(bar.p_full + t, 128);
+            mbar_init(bar.o_full + t, 1);
+        }
+        mbar_init(bar.drain, 1);
+#pragma unroll
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar.k_full + s, 1);
+            mbar_init(bar.k_empty + s, 1);
+            mbar_init(bar.v_full + s, 1);
+            mbar_init(bar.v_empty + s, 1);
+        }
+        *bar.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(bar.tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *bar.tmem_slot;
+    int *status = p.ws.status;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const uint64_t pol_kv = policy_evict_last();
+            const uint64_t pol_q = policy_evict_first();
+            uint32_t q_uses[2] = {0, 0};
+            uint32_t g = 0;        // key tiles started by this CTA
+            uint32_t gk = 0, gv = 0;  // K / V copies issued
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
+                const int4 U = p.units[unit_index(p, i)];
+                const int e0 = p.row_ptr[U.y], e1 = p.row_ptr[U.y + 1];
+                const int nkv = (e1 - e0) * tpb;
+                if (nkv == 0) continue;
+                for (int t = 0; t < U.w && ok; ++t) {
+                    ok = mbar_wait(bar.q_empty + t, (q_uses[t] & 1) ^ 1, bar.abort, status, kStatusTimeout, tmo);
+                    if (!ok) break;
+                    ++q_uses[t];
+                    mbar_arrive_expect_tx(bar.q_full + t, C::Q_TILE);
+#pragma unroll
+                    for (int h = 0; h < C::DH; ++h)
+                        tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + h * C::HALF_Q, &tm_q, h * 64,
+                                    (U.z + t) * kQTile, U.x * p.nb + U.y, bar.q_full + t, pol_q);
+                }
+                for (int j = 0; j < nkv && ok; ++j, ++g) {
+                    const int kb = p.col_idx[e0 + j / tpb];
+                    const int row = static_cast<int>(static_cast<int64_t>(U.x) * p.L +
+                                                     static_cast<int64_t>(kb) * p.block) +
+                                    (j % tpb) * N;
+                    const int s = static_cast<int>(g % C::STAGES);
+                    const uint32_t ph = (g / C::STAGES) & 1;
+                    ok = mbar_wait(bar.k_empty + s, ph ^ 1, bar.abort, status, kStatusTimeout, tmo);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar.k_full + s, C::KV_TILE);
+#pragma unroll
+                    for (int h = 0; h < C::DH; ++h)
+                        tma_load_2d(smem + C::OFF_K + s * C::KV_TILE + h * C::HALF_KV, &tm_k, h * 64, row,
+                                    bar.k_full + s, pol_kv);
+                    ++gk;
+                    ok = mbar_wait(bar.v_empty + s, ph ^ 1, bar.abort, status, kStatusTimeout, tmo);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar.v_full + s, C::KV_TILE);
+#pragma unroll
+                    for (int h = 0; h < C::DH; ++h)
+                        tma_load_2d(smem + C::OFF_V + s * C::KV_TILE + h * C::HALF_KV, &tm_v, h * 64, row,
+                                    bar.v_full + s, pol_kv);
+                    ++gv;
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA's shared memory goes away.
+                for (int t = 0; t < 2; ++t)
+                    if (q_uses[t]) mbar_drain(bar.q_full + t, (q_uses[t] - 1) & 1, tmo);
+                for (uint32_t x = (gk > C::STAGES ? gk - C::STAGES : 0); x < gk; ++x)
+                    mbar_drain(bar.k_full + x % C::STAGES, (x / C::STAGES) & 1, tmo);
+                for (uint32_t x = (gv > C::STAGES ? gv - C::STAGES : 0); x < gv; ++x)
+                    mbar_drain(bar.v_full + x % C::STAGES, (x / C::STAGES) & 1, tmo);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+            const uint32_t k_base = smem_u32(smem + C::OFF_K);
+            const uint32_t v_base = smem_u32(smem + C::OFF_V);
+            auto issue_qk = [&](int t, int s) {
+                const uint32_t qa = q_base + t * C::Q_TILE;
+                const uint32_t ka = k_base + s * C::KV_TILE;
+                const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * C::HALF_Q + off, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * C::HALF_KV + off, 16, 1024);
+                    mma_ss(d, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+                const uint32_t va = v_base + s * C::KV_TILE;
+                const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
+                const uint32_t a = tmem + (t ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(va + kk * 16 * 128, C::HALF_KV, 1024);
+                    mma_ts(d, a + kk * 8, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0};
+            uint32_t g = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
+                const int4 U = p.units[unit_index(p, i)];
+                const int nkv = (p.row_ptr[U.y + 1] - p.row_ptr[U.y]) * tpb;
+                if (nkv == 0) continue;
+                const int nt = U.w;
+                for (int t = 0; t < nt && ok; ++t) {
+                    ok = mbar_wait(bar.q_full + t, q_uses[t] & 1, bar.abort, status, kStatusTimeout, tmo);
+                    ++q_uses[t];
+                }
+                if (!ok) break;
+                {
+                    const int s0 = static_cast<int>(g % C::STAGES);
+                    ok = mbar_wait(bar.k_full + s0, (g / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int t = 0; t < nt; ++t) {
+                        issue_qk(t, s0);
+                        mma_commit(bar.s_full + t);
+                        if (nkv == 1) mma_commit(bar.q_empty + t);
+                    }
+                    mma_commit(bar.k_empty + s0);
+                }
+                for (int j = 0; j < nkv && ok; ++j) {
+                    const uint32_t gj = g + j, gn = g + j + 1;
+                    const int sj = static_cast<int>(gj % C::STAGES), sn = static_cast<int>(gn % C::STAGES);
+                    const bool more = j + 1 < nkv;
+                    ok = mbar_wait(bar.v_full + sj, (gj / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
+                    if (ok && more)
+                        ok = mbar_wait(bar.k_full + sn, (gn / C::STAGES) & 1, bar.abort, status, kStatusTimeout,
+                                       tmo);
+                    for (int t = 0; t < nt && ok; ++t) {
+                        ok = mbar_wait(bar.p_full + t, p_uses[t] & 1, bar.abort, status, kStatusTimeout, tmo);
+                        if (!ok) break;
+                        ++p_uses[t];
+                        tc_fence_after();
+                        issue_pv(t, sj, j > 0);
+                        if (more) {
+                            issue_qk(t, sn);
+                            mma_commit(bar.s_full + t);
+                            if (j + 2 == nkv) mma_commit(bar.q_empty + t);
+                        } else {
+                            mma_commit(bar.o_full + t);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar.v_empty + sj);
+                    if (more) mma_commit(bar.k_empty + sn);
+                }
+                g += nkv;
+            }
+            // Every MMA issued must complete before TMEM is freed.
+            mma_commit(bar.drain);
+            mbar_drain(bar.drain, 0, tmo);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- softmax + epilogue
+        const int t = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
+        const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+        const float c1 = p.scale_log2;
+        uint32_t s_uses = 0, o_uses = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
+            const int u = unit_index(p, i);
+            const int4 U = p.units[u];
+            if (t >= U.w) continue;
+            const int nkv = (p.row_ptr[U.y + 1] - p.row_ptr[U.y]) * tpb;
+            const int qt = U.z + t;
+            const int rows_valid = min(kQTile, p.block - qt * kQTile);
+            const bool valid = r < rows_valid;
+            const int64_t grow = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
+                                 static_cast<int64_t>(qt) * kQTile + r;
+            uint16_t *orow = p.o + grow * D;
+            if (nkv == 0) {  // the frame reads no key block: O = 0, LSE = -inf
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[grow] = -INFINITY;
+                }
+                continue;
+            }
+            float mrow;  // bound: m_i (natural units); online: running max in log2 units
+            float m2;
+            if constexpr (ONLINE) {
+                mrow = -INFINITY;
+                m2 = 0.0f;
+            } else {
+                mrow = valid ? p.rowbound[grow] : 0.0f;
+                m2 = mrow * 1.4426950408889634f;
+            }
+            float l0 = 0.0f, l1 = 0.0f;
+            for (int j = 0; j < nkv; ++j) {
+                ok = mbar_wait(bar.s_full + t, s_uses & 1, bar.abort, status, kStatusTimeout, tmo);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                ++s_uses;
+                tc_fence_after();
+                if constexpr (ONLINE) {
+                    const float mx = tile_row_max<N>(tS) * c1;
+                    if (j == 0) {
+                        mrow = mx;
+                    } else {
+                        // Rescale only when the max grew by more than 2^8: a stale max
+                        // keeps P <= 2^8, exact in fp32 and bf16.
+                        const bool need = mx > mrow + 8.0f;
+                        if (__any_sync(0xFFFFFFFFu, need)) {
+                            const float alpha = need ? ex2_approx(mrow - mx) : 1.0f;
+                            if (need) mrow = mx;
+                            l0 *= alpha;
+                            l1 *= alpha;
+                            rescale_o_row<D>(tO, alpha);
+                        }
+                    }
+                    m2 = mrow;
+                }
+                softmax_tile_bound<N>(tS, c1, m2, l0, l1);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar.p_full + t);
+            }
+            if (!ok) break;
+            ok = mbar_wait(bar.o_full + t, o_uses & 1, bar.abort, status, kStatusTimeout, tmo);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ++o_uses;
+            tc_fence_after();
+            const float l = l0 + l1;
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[16], b[16];
+                tmem_ld16(tO + c * 32, a);
+                tmem_ld16(tO + c * 32 + 16, b);
+                tmem_wait_ld();
+                reg_fence16(a);
+                reg_fence16(b);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * inv, __uint_as_float(a[2 * e + 1]) * inv);
+                    w[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]) * inv, __uint_as_float(b[2 * e + 1]) * inv);
+                }
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
+            }
+            if (valid && p.lse) {
+                if constexpr (ONLINE)
+                    p.lse[grow] = (mrow + log2f(l)) * 0.6931471805599453f;
+                else
+                    p.lse[grow] = mrow + logf(l);
+            }
+            if constexpr (!ONLINE) {
+                if (p.mode == kModeBound) {
+                    // Underflow guard: a denominator below 2^-64 (or not finite) means the bound was
+                    // too loose for exp to resolve this row; rerun its unit with the online max.
+                    const bool bad = valid && !(l >= kGuardTau && l <= 3.402823466e38f);
+                    const unsigned ballot = __ballot_sync(0xFFFFFFFFu, bad);
+                    if (ballot && lane == 0) {
+                        atomicAdd(p.ws.fb_rows, __popc(ballot));
+                        if (atomicExch(p.ws.unit_flag + u, 1) == 0) {
+                            const int pos = atomicAdd(p.ws.fb_count, 1);
+                            p.ws.fb_list[pos] = u;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, int N, bool ONLINE>
+cudaError_t launch_fwd_instance(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                const AttnParams &p, int n_ctas, cudaStream_t s) {
+    bsattn_fwd_kernel<D, N, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D, N>::SMEM, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <int D, int N>
+cudaError_t configure_instance() {
+    cudaError_t e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttnCfg<D, N>::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(bsattn_fwd_kernel<D, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                AttnCfg<D, N>::SMEM);
+}
+
+}  // namespace bsv

@@ -1,0 +1,77 @@
+// Internal interfaces between the C-ABI host code (api.cpp) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsv {
+
+constexpr int kQTile = 128;           // query rows per tile (the MMA M dimension)
+constexpr int kMaxKvTile = 128;       // keys per tile, upper bound (TMEM: 2 S + 2 O accumulators)
+constexpr int kAttnThreads = 384;     // 12 warps: TMA, MMA, 2 idle, 2 softmax warpgroups
+constexpr float kGuardTau = 5.421010862427522e-20f;  // 2^-64: smallest denominator trusted
+constexpr int kStatusTimeout = 1;     // bit in the device status word
+
+// Device-side workspace of a layout (one allocation, zeroed per forward where noted).
+struct Workspace {
+    int32_t *fb_count;   // units appended to the fallback list      (zeroed per forward)
+    int32_t *fb_rows;    // rows flagged by the guard                  (zeroed per forward)
+    int32_t *status;     // device status bits (kStatusTimeout)        (zeroed at create)
+    int32_t *unit_flag;  // per work unit: flagged already             (zeroed per forward)
+    int32_t *fb_list;    // work-unit indices to rerun
+};
+
+enum AttnMode : int32_t {
+    kModeBound = 0,     // bound softmax over every unit, guard on
+    kModeOnlineAll = 1, // online max over every unit
+    kModeFallback = 2   // online max over the units listed in fb_list[0 .. *fb_count)
+};
+
+struct AttnParams {
+    const int4 *units;        // (b*H + h, qb, first q tile, tiles in unit)
+    int32_t n_units;
+    const int32_t *row_ptr;   // allowed key blocks per query block (CSR)
+    const int32_t *col_idx;
+    const float *rowbound;    // [B*H*L]
+    uint16_t *o;              // [B*H*L, D] bf16 bits
+    float *lse;               // [B*H*L] or null
+    Workspace ws;
+    int64_t L;
+    int32_t block;            // tokens per frame block
+    int32_t nb;
+    float scale_log2;         // scale * log2(e)
+    int32_t mode;
+    uint64_t timeout_ns;
+};
+
+struct BoundsParams {
+    const uint16_t *q, *k;
+    float *qnorm;
+    uint32_t *kmax_bits;      // fp32 bits, zeroed before the norms launch
+    float *rowbound;
+    const int32_t *row_ptr, *col_idx;
+    int64_t L;
+    int32_t block, nb, BH;
+    int32_t chunks_per_block; // row chunks per frame block
+    float scale;
+};
+
+// Launchers (return the launch error, if any).
+cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s);
+cudaError_t launch_rowbound(const BoundsParams &p, cudaStream_t s);
+int bounds_chunk_rows();
+
+// Attention kernel for head dim D and key tile N; grid = n_ctas persistent CTAs.
+cudaError_t launch_attention_d64(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const AttnParams &p, int N, bool online, int n_ctas, cudaStream_t s);
+cudaError_t launch_attention_d128(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                  const AttnParams &p, int N, bool online, int n_ctas, cudaStream_t s);
+// Raise the dynamic shared-memory limit of both variants for (D, N).
+cudaError_t configure_attention_d64(int N);
+cudaError_t configure_attention_d128(int N);
+// Dynamic shared memory of one CTA for (D, N).
+size_t smem_attention_d64(int N);
+size_t smem_attention_d128(int N);
+
+}  // namespace bsv

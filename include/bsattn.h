@@ -1,0 +1,190 @@
+/*
+ * bsattn.h -- C ABI of the frame-aligned block-sparse attention forward for
+ * B300 (sm_103a).  Library: libbsattn.so (block_sparse_video_row_b300/).
+ *
+ * The operation (web pages on HeyGen's Avatar IV port to Trillium TPUs):
+ *  - Attention in a video super-resolution transformer whose block mask, at
+ *    frame granularity, says which key/value blocks each query block reads.
+ *    Block edges coincide with frame edges and the block size is any multiple
+ *    of 16, so no element predicate, tail pass or padding exists
+ *    ("HeyGen Avatar IV on Trillium TPU" deep-dive, section 把 block 縮到 16 /
+ *    "shrink the block to 16"; "Optimizing HeyGen's Avatar IV diffusion model
+ *    for Google Cloud TPUs", section "How it works").
+ *  - The softmax uses a precomputed per-row upper bound on the logits in place
+ *    of the running max: m_i = scale * |q_i| * max over allowed keys |k_j|,
+ *    which holds by Cauchy-Schwarz, so exp(S - m_i) accumulates with no
+ *    rescaling (deep-dive, section 拿掉 softmax 的序列相依 / "remove softmax's
+ *    serial dependency"; "How is HeyGen optimizing AI video on Google Cloud
+ *    TPUs", section "Innovating Beyond Serial Dependencies").  Rows where the
+ *    bound is so loose that the exponentials underflow are detected and rerun
+ *    with a running-max (online softmax) kernel (the deep-dive's per-head
+ *    eligibility check with fallback to online softmax, same section).
+ *
+ * Tensors: Q, K, V, O are bf16, contiguous [B, H, L, D], L = nb * block_size,
+ * 16-byte-aligned base addresses, on the device that was current at
+ * bsattn_create_layout.  Row i of head (b, h) belongs to block i / block_size.
+ * The block mask is one [nb, nb] uint8 matrix (row-major, nonzero = query block
+ * qb reads key block kb), shared by every batch entry and head.  L_q = L_kv.
+ *
+ * Ownership: the caller owns every tensor it passes (Q, K, V, O, LSE and the
+ * metadata buffers).  A layout owns its host plan and its device buffers (the
+ * allowed-block table, the work list and a small workspace for the underflow
+ * guard), allocated by bsattn_create_layout and freed by bsattn_destroy.  The
+ * mask is copied; the caller may free it after create.
+ *
+ * Streams: bsattn_row_bounds and bsattn_forward enqueue work on `stream` and
+ * never synchronise.  A layout keeps per-call state in its workspace, so calls
+ * with the same layout must not overlap on the GPU (use one stream per layout).
+ *
+ * Errors: argument errors are returned before any work is enqueued.  Device-
+ * side conditions (a bounded wait that ran out, which the kernel reports and
+ * returns from instead of hanging) are recorded in a device status word that
+ * bsattn_query_stats returns.
+ */
+#ifndef BSATTN_H
+#define BSATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, passed through unchanged (NULL = the legacy default stream). */
+typedef struct CUstream_st *bsattn_stream_t;
+
+typedef struct bsattn_layout_s *bsattn_layout_t;
+
+typedef enum {
+    BSATTN_OK = 0,
+    BSATTN_ERR_INVALID_ARG = 1,     /* null pointer, bad size, misaligned pointer, plan-only layout */
+    BSATTN_ERR_UNALIGNED_BLOCK = 2, /* block_size not a multiple of 16, or L not a multiple of it */
+    BSATTN_ERR_UNSUPPORTED = 3,     /* D other than 64 or 128, or sizes beyond the limits below */
+    BSATTN_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
+    BSATTN_ERR_OOM = 5,             /* device allocation failed at create */
+    BSATTN_ERR_TIMEOUT = 6,         /* a bounded device wait ran out (reported by query_stats) */
+    BSATTN_ERR_DEVICE = 7           /* no usable sm_100-family device */
+} bsattn_status;
+
+/* flags */
+enum {
+    /* bsattn_forward: bound softmax + underflow guard + online-max rerun of
+       flagged work units (the default). */
+    BSATTN_BOUND = 0,
+    /* bsattn_forward: run the online-max (running max + rescale) kernel over
+       every work unit instead; the A/B baseline of the same kernel. */
+    BSATTN_ONLINE_MAX = 1,
+    /* bsattn_forward: skip the rerun of flagged units (testing only: rows
+       whose exponentials underflowed keep an undefined value). */
+    BSATTN_NO_FALLBACK = 2,
+    /* bsattn_create_layout: build the host plan only, touch no device; such a
+       layout can be inspected (info/export) but not run. */
+    BSATTN_PLAN_ONLY = 0x10
+};
+
+/* Limits checked by bsattn_create_layout. */
+#define BSATTN_MAX_NB 4096            /* frames (blocks) per sequence */
+#define BSATTN_MAX_ROWS 2147483647LL  /* B * H * L */
+
+/*
+ * Build a layout for one problem shape and block mask.
+ *   out         receives the handle (set to NULL on error).
+ *   B, H        batch and heads (>= 1).
+ *   L           tokens per sequence (frames x tokens per frame), a multiple of block_size.
+ *   D           head dimension: 64 or 128.
+ *   block_size  tokens per frame block: a multiple of 16 (>= 16).
+ *   block_mask  host pointer, nb * nb bytes, nb = L / block_size.
+ *   flags       0, or BSATTN_PLAN_ONLY.
+ * The plan: the allowed key blocks of each query block in ascending order;
+ * the key tile (the largest multiple of 16 that divides block_size, at most
+ * 128, so tiles never straddle a frame edge); query tiles of 128 rows that
+ * never straddle a frame edge (the last tile of a frame may be partial); and a
+ * work list of pairs of query tiles of one frame, sorted by cost, largest first.
+ * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA, OOM or DEVICE.
+ */
+bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,
+                                   int32_t block_size, const uint8_t *block_mask, int32_t flags);
+
+/*
+ * The Cauchy-Schwarz row bounds (the precomputed norm table of the deep-dive,
+ * section 拿掉 softmax 的序列相依).  All pointers are device pointers.
+ *   q, k      bf16 [B, H, L, D].
+ *   scale     the softmax scale (usually 1/sqrt(D)); pass the same value to bsattn_forward.
+ *   qnorm     out, fp32 [B, H, L]: |q_i|.
+ *   kmax      out, fp32 [B, H, nb]: the largest |k_j| of each key block.
+ *   rowbound  out, fp32 [B, H, L]: m_i = (scale * |q_i|) * max over allowed kb of kmax[kb],
+ *             each product rounded to fp32 (0 for a row that reads no block).
+ * Norms use one fixed fp32 rounding order: the D elements split into 16
+ * contiguous chunks, fmaf over each chunk in order, the chunk sums combined
+ * pairwise at distances 8, 4, 2, 1, then a correctly rounded sqrt; so the
+ * results are reproducible bit for bit.  Enqueued on `stream`; returns
+ * BSATTN_OK, INVALID_ARG or CUDA.
+ */
+bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *k, float scale,
+                                float *qnorm, float *kmax, float *rowbound, bsattn_stream_t stream);
+
+/*
+ * The attention forward.  All pointers are device pointers.
+ *   q, k, v   bf16 [B, H, L, D] in.
+ *   o         bf16 [B, H, L, D] out (every row is written; rows that read no block get 0).
+ *   scale     softmax scale (the value given to bsattn_row_bounds).
+ *   rowbound  fp32 [B, H, L] from bsattn_row_bounds (unused with BSATTN_ONLINE_MAX; may be NULL then).
+ *   lse       optional fp32 [B, H, L] out: the natural log of the softmax denominator,
+ *             ln sum_j exp(scale * q_i . k_j) over allowed keys (-inf for rows that read nothing).
+ *   flags     BSATTN_BOUND (0), BSATTN_ONLINE_MAX, and/or BSATTN_NO_FALLBACK.
+ * BSATTN_BOUND computes P = exp(scale * S - m_i) with no running max, rounds P
+ * to bf16 for the P.V product and sums the denominator from the same rounded
+ * values; a row is flagged when its denominator is below 2^-64 or not finite,
+ * and every work unit holding a flagged row is recomputed by the online-max
+ * kernel in a second launch on the same stream (no host synchronisation).
+ * Enqueued on `stream`; returns BSATTN_OK, INVALID_ARG or CUDA.
+ */
+bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, const void *v, void *o,
+                             float scale, const float *rowbound, float *lse, int32_t flags,
+                             bsattn_stream_t stream);
+
+/* Free the layout's device buffers and host plan.  NULL is ignored. */
+void bsattn_destroy(bsattn_layout_t lay);
+
+/* ---- helpers ----------------------------------------------------------------------------- */
+
+/* A static, human-readable name for a status code. */
+const char *bsattn_status_string(bsattn_status st);
+
+/*
+ * Statistics of the last bsattn_forward on this layout.  Synchronises `stream`.
+ *   fallback_rows   rows flagged by the underflow guard (nullable).
+ *   fallback_units  work units rerun with the online-max kernel (nullable).
+ *   device_status   BSATTN_OK, or BSATTN_ERR_TIMEOUT if a bounded device wait
+ *                   ran out since the layout was created (nullable).
+ */
+bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, int64_t *fallback_units,
+                                 int32_t *device_status, bsattn_stream_t stream);
+
+/* Plan summary of a layout (host only). */
+typedef struct {
+    int32_t B, H, D, block_size, nb;
+    int64_t L;
+    int32_t nnz_blocks;        /* allowed (query block, key block) pairs */
+    int32_t kv_tile;           /* keys per tile */
+    int32_t q_tiles_per_block; /* ceil(block_size / 128) */
+    int32_t n_units;           /* work units (pairs of query tiles of one frame) */
+    int64_t mma_rows;          /* query rows the MMAs process, partial tiles included */
+    double useful_flop;        /* 4 * nnz_blocks * block_size^2 * D * H * B */
+} bsattn_layout_info_t;
+
+bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info);
+
+/*
+ * Copy the plan to host arrays (any may be NULL):
+ *   row_ptr  int32 [nb + 1], col_idx int32 [nnz_blocks]: allowed key blocks per query block, ascending;
+ *   units    int32 [n_units * 4]: (b * H + h, query block, first query tile, tiles in the unit (1 or 2)),
+ *            in execution order.
+ */
+bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSATTN_H */

@@ -1,0 +1,132 @@
+"""Host-side logic of the C ABI, on CPU: exported symbols, the plan, argument checks.
+
+No compute call is made here (there may be no GPU): plan-only layouts are inspected
+and every error path that returns before touching a device is exercised.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from block_sparse_video_row_b300 import _build, bsattn, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return bsattn.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "bsattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsattn_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert set(declared) == set(bsattn.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def _expected_kv_tile(bs):
+    return max(n for n in range(16, 129, 16) if bs % n == 0)
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_plan_matches_oracle(lib, name):
+    w = synth.WORKLOADS[name]
+    mask = w.block_mask()
+    lay = bsattn.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, bsattn.BSATTN_PLAN_ONLY)
+    info = lay.info
+    row_ptr, col_idx, units = bsattn.bsattn_layout_export(lay)
+    orp, oci = oracle.allowed_csr(mask)
+    assert np.array_equal(row_ptr, orp) and np.array_equal(col_idx, oci)
+    assert info.nnz_blocks == len(oci) and info.nb == w.nb
+    assert info.kv_tile == _expected_kv_tile(w.block)
+    assert w.block % info.kv_tile == 0 and info.kv_tile % 16 == 0
+    nqt = -(-w.block // 128)
+    assert info.q_tiles_per_block == nqt
+    assert abs(info.useful_flop - synth.useful_flop(w)) == 0
+    # every (head, frame, query tile) exactly once; units are 1 or 2 tiles of one frame
+    seen = np.zeros((w.B * w.H, w.nb, nqt), np.int32)
+    for bh, qb, qt0, nt in units:
+        assert nt in (1, 2) and qt0 % 2 == 0 and qt0 + nt <= nqt
+        seen[bh, qb, qt0:qt0 + nt] += 1
+    assert np.all(seen == 1)
+    # largest cost first
+    nkv = np.diff(orp)[units[:, 1]] * (w.block // info.kv_tile)
+    cost = nkv * units[:, 3]
+    assert np.all(np.diff(cost) <= 0)
+    lay.destroy()
+
+
+def test_plan_edge_shapes(lib):
+    # single frame of 16 tokens; a frame that reads nothing; ragged 128-row tiles
+    for (L, bs) in [(16, 16), (48, 16), (400, 400), (1040, 208), (272, 272)]:
+        nb = L // bs
+        mask = np.ones((nb, nb), np.uint8)
+        if nb > 1:
+            mask[1, :] = 0
+        lay = bsattn.bsattn_create_layout(2, 3, L, 64, bs, mask, bsattn.BSATTN_PLAN_ONLY)
+        assert lay.info.kv_tile == _expected_kv_tile(bs)
+        _, _, units = bsattn.bsattn_layout_export(lay)
+        assert len(units) == lay.info.n_units == 6 * nb * ((-(-bs // 128) + 1) // 2)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 1, 192, 64, 40), bsattn.BSATTN_ERR_UNALIGNED_BLOCK),     # block not a multiple of 16
+    ((1, 1, 200, 64, 48), bsattn.BSATTN_ERR_UNALIGNED_BLOCK),     # L not a multiple of block
+    ((1, 1, 192, 96, 48), bsattn.BSATTN_ERR_UNSUPPORTED),         # head dim 96
+    ((0, 1, 192, 64, 48), bsattn.BSATTN_ERR_INVALID_ARG),         # B = 0
+    ((1, 1, 192, 64, 0), bsattn.BSATTN_ERR_INVALID_ARG),          # block 0
+    ((1, 1, 16 * 5000, 64, 16), bsattn.BSATTN_ERR_UNSUPPORTED),   # too many frames
+    ((40000, 64, 1024, 64, 16 * 64), bsattn.BSATTN_ERR_UNSUPPORTED),  # B*H*L beyond int32
+])
+def test_create_rejects_bad_arguments(lib, args, status):
+    B, H, L, D, bs = args
+    nb = max(L // bs, 1) if bs else 1
+    mask = np.ones((min(nb, 5000), min(nb, 5000)), np.uint8)
+    st, lay = bsattn.bsattn_create_layout(B, H, L, D, bs, mask, bsattn.BSATTN_PLAN_ONLY, raise_on_error=False)
+    assert st == status and lay is None
+
+
+def test_create_rejects_null_mask_and_bad_flags(lib):
+    import ctypes
+    h = ctypes.c_void_p()
+    assert lib.bsattn_create_layout(ctypes.byref(h), 1, 1, 192, 64, 48, None, 0) == bsattn.BSATTN_ERR_INVALID_ARG
+    assert h.value is None
+    m = np.ones((4, 4), np.uint8)
+    assert lib.bsattn_create_layout(ctypes.byref(h), 1, 1, 192, 64, 48, m.ctypes.data, 0x4) == \
+        bsattn.BSATTN_ERR_INVALID_ARG
+    assert lib.bsattn_create_layout(None, 1, 1, 192, 64, 48, m.ctypes.data, 0) == bsattn.BSATTN_ERR_INVALID_ARG
+
+
+def test_plan_only_layout_refuses_device_calls(lib):
+    lay = bsattn.bsattn_create_layout(1, 2, 192, 64, 48, synth.window_mask(4, 1), bsattn.BSATTN_PLAN_ONLY)
+    fake = 1 << 20  # never dereferenced: the plan-only check comes first
+    assert bsattn.bsattn_row_bounds(lay, fake, fake, 0.125, fake, fake, fake, 0, raise_on_error=False) == \
+        bsattn.BSATTN_ERR_INVALID_ARG
+    assert bsattn.bsattn_forward(lay, fake, fake, fake, fake, 0.125, fake, None, 0, 0, raise_on_error=False) == \
+        bsattn.BSATTN_ERR_INVALID_ARG
+    lay.destroy()
+    lib.bsattn_destroy(None)  # NULL is ignored
+
+
+def test_status_strings(lib):
+    for st in range(8):
+        assert isinstance(bsattn.status_string(st), str) and bsattn.status_string(st)
+    assert bsattn.status_string(99) == "unknown status"
+
+
+def test_device_layout_without_gpu_reports_an_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, lay = bsattn.bsattn_create_layout(1, 2, 192, 64, 48, synth.window_mask(4, 1), 0, raise_on_error=False)
+    assert st in (bsattn.BSATTN_ERR_DEVICE, bsattn.BSATTN_ERR_CUDA) and lay is None
