@@ -1,0 +1,329 @@
+#!/usr/bin/env python
+"""Benchmark: frame-aligned block-sparse attention forward (bf16) on B300.
+
+One step = the whole hot path over one synthetic 720p latent chunk
+(B=1, H=24, L=13x3600=46800, D=128, window +-1 frame plus the first frame):
+bsattn_row_bounds (norms + Cauchy-Schwarz row bounds) then bsattn_forward
+(bound-softmax attention, underflow guard, online-max rerun of flagged units).
+
+Prints ONE JSON line.  value = useful TFLOP/s = 4 * sum_allowed(block^2) * D * H * B
+per step / device time per step (inputs resident in HBM, CUDA events on the
+launching stream); e2e = the same metric with pinned host buffers and the
+host<->device copies inside the timed region.  --impl reference times the fp64
+CPU oracle (the reference arm of this build) on a bounded sample of the same
+workload.  Multi-GPU: one process per GPU under torchrun, each rank runs its
+own chunk (independent problems, no collective on the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "useful TFLOP/s block-sparse attn fwd (bf16) on 1 B300; % of tensor peak"
+UNIT = "TFLOP/s"
+
+
+def _env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(q, k, v, w, seconds: float, seed: int = 1):
+    """Time the fp64 oracle on a bounded random sample of query rows; returns (TFLOP/s, rows, secs, cores)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    mask = w.block_mask()
+    allowed_keys = mask.sum(axis=1) * w.block  # per query frame
+    n_total = w.B * w.H * w.L
+
+    def run(nrows):
+        rows = np.sort(rng.choice(n_total, size=nrows, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, mask, w.block, w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        frames = (rows % w.L) // w.block
+        flop = float(np.sum(4.0 * allowed_keys[frames] * w.D))
+        return flop, dt
+
+    cores = oracle.n_threads()
+    flop, dt = run(max(cores * 4, 32))
+    nrows = int(min(n_total, max(cores * 4, (cores * 4) * seconds / max(dt, 1e-3))))
+    flop, dt = run(nrows)
+    return flop / dt / 1e12, nrows, dt, cores
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="720p")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0, help="override H (a smaller case of the same shape, for ncu)")
+    ap.add_argument("--profile", action="store_true",
+                    help="run only W warm-up and K timed steps (a short, fixed launch sequence for ncu)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, local_rank = _env_rank()
+    from block_sparse_video_row_b300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.heads:
+        w = synth.Workload(f"{w.name}-h{args.heads}", w.B, args.heads, w.D, w.frames, w.block, w.mask, w.keys, w.seed)
+    flop_step = synth.useful_flop(w)
+    config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D, "frames": w.frames,
+              "block": w.block, "mask": "frame window" + (" + first frame" if w.block_mask()[-1, 0] else ""),
+              "nnz_blocks": int(w.block_mask().sum()), "keys": w.keys, "seed": w.seed,
+              "useful_flop_per_step": flop_step,
+              "l2": "inputs larger than L2 (Q+K+V+O %.2f GB > 126 MB), no flush" % (4 * w.B * w.H * w.L * w.D * 2 / 1e9)}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        q, k, v = synth.make_qkv(w)
+        times, flops, rows_total = [], [], 0
+        per_step = max(1.0, args.cpu_seconds / max(args.steps, 1))
+        for i in range(args.warmup + args.steps):
+            tf, nrows, dt, cores = cpu_oracle_sample(q, k, v, w, per_step if i >= args.warmup else 0.2, seed=i)
+            if i >= args.warmup:
+                times.append(dt)
+                flops.append(tf)
+                rows_total += nrows
+        val = float(np.median(flops))
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.median(times)) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                 "sample": f"{rows_total} random query rows over {args.steps} steps "
+                                           f"(~{per_step:.1f} s of fp64 CPU work each)"},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as dist
+    from block_sparse_video_row_b300 import _build, bsattn
+
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    _build.build()
+    bsattn.load()
+
+    q, k, v = synth.make_qkv(w)
+    # each rank gets an independent chunk of the same shape (weak scaling)
+    if rank > 0:
+        wr = synth.Workload(w.name, w.B, w.H, w.D, w.frames, w.block, w.mask, w.keys, seed=w.seed + rank)
+        q, k, v = synth.make_qkv(wr)
+
+    def pinned(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = pinned(q), pinned(k), pinned(v)
+    dq, dk, dv = hq.cuda(), hk.cuda(), hv.cuda()
+    B, H, L, D = q.shape
+    nb = L // w.block
+    o = torch.empty_like(dq)
+    ho = torch.empty_like(hq).pin_memory()
+    qn = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    km = torch.empty((B, H, nb), dtype=torch.float32, device="cuda")
+    rb = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    lay = bsattn.bsattn_create_layout(B, H, L, D, w.block, w.block_mask())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        bsattn.bsattn_row_bounds(lay, dq, dk, w.scale, qn, km, rb, stream)
+        bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None, bsattn.BSATTN_BOUND, stream)
+
+    def timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    if args.profile:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        lay.destroy()
+        print(json.dumps({"profile_run": w.name, "steps": args.warmup + args.steps, "kernels_per_step": 4}))
+        return
+
+    # ---- warm-up: W steps, continued until the clock sampler (started now) is running under load
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t0, n_warm = time.time(), 0
+    while n_warm < args.warmup or time.time() - t0 < 0.8:
+        step()
+        torch.cuda.synchronize()
+        n_warm += 1
+    fb_rows, fb_units, dev_status = bsattn.bsattn_query_stats(lay, stream)
+
+    # ---- main timed region: K steps, barrier + synchronize on both sides, clocks sampled meanwhile
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = flop_step * world / (ms_step * 1e-3) / 1e12
+
+    # ---- the dominant kernel alone (bound attention, no rerun launch), and the online-max A/B variant
+    attn_ms = timed(lambda: bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None,
+                                                  bsattn.BSATTN_NO_FALLBACK, stream), max(args.steps, 5))
+    online_ms = timed(lambda: bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None,
+                                                    bsattn.BSATTN_ONLINE_MAX, stream), max(args.steps, 5))
+    bounds_ms = timed(lambda: bsattn.bsattn_row_bounds(lay, dq, dk, w.scale, qn, km, rb, stream),
+                      max(args.steps, 5))
+    attn_avg = float(np.mean(attn_ms))
+    peaks, peak_src = _peaks()
+    achieved = flop_step / (attn_avg * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        tj = json.load(open(prof))
+        if tj.get("workload") == w.name and tj.get("kernel_rev") == bsattn_kernel_rev():
+            traffic = tj.get("dram_bytes_per_launch")
+    roofline = {"bound": "tensor", "kernel": "bsattn_fwd_kernel<128,%d,bound>" % lay.info.kv_tile,
+                "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense (burst; sustained {peaks.get('bf16_tflops_sustained')})",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "launch_ms": attn_avg}
+
+    # ---- end to end: pinned host buffers, H2D of Q,K,V + bounds + forward + D2H of O each step
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+
+    e2e_ms = timed(e2e_step, max(3, args.steps // 4))
+    e2e_val = flop_step * world / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
+
+    launches_per_step = 4  # norms, rowbound, bound attention, rerun of flagged units
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "pct_of_tensor_peak": 100.0 * value / world / peak,
+            "roofline": roofline,
+            "e2e": {"value": e2e_val, "unit": UNIT, "ms_per_step": float(np.mean(e2e_ms)),
+                    "h2d_bytes_per_step": 3 * int(dq.numel()) * 2, "d2h_bytes_per_step": int(o.numel()) * 2},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "ab": {"bound_attn_ms": attn_avg, "online_max_attn_ms": float(np.mean(online_ms)),
+                   "bound_speedup_vs_online": float(np.mean(online_ms)) / attn_avg,
+                   "row_bounds_ms": float(np.mean(bounds_ms))},
+            "guard": {"fallback_rows": fb_rows, "fallback_units": fb_units, "device_status": dev_status},
+            "wasted_mma_rows_pct": 100.0 * (lay.info.mma_rows - B * H * L) / lay.info.mma_rows}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, nrows, dt, cores = cpu_oracle_sample(q, k, v, w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{nrows} random query rows of the {w.name} chunk, {dt:.1f} s fp64"}
+    lay.destroy()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bsattn_kernel_rev() -> str:
+    """Hash of the attention kernel source: a stored ncu traffic figure is used only for this exact kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_kernel.cuh", "ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "block_sparse_video_row_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()
