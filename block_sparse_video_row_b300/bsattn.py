@@ -35,7 +35,8 @@ BSATTN_NO_FALLBACK = 2
 BSATTN_PLAN_ONLY = 0x10
 
 EXPORTED = ("bsattn_create_layout", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
-            "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export")
+            "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export",
+            "bsattn_forward_noalloc")
 
 
 class LayoutInfo(ctypes.Structure):
@@ -82,6 +83,8 @@ def load(path: Optional[str] = None):
     lib.bsattn_query_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i32), vp]
     lib.bsattn_layout_info.restype = i32
     lib.bsattn_layout_info.argtypes = [vp, ctypes.POINTER(LayoutInfo)]
+    lib.bsattn_forward_noalloc.restype = i32
+    lib.bsattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, i32, vp, f32, vp, vp, i32, vp]
     lib.bsattn_layout_export.restype = i32
     lib.bsattn_layout_export.argtypes = [vp, vp, vp, vp]
     _lib = lib
@@ -176,6 +179,19 @@ def bsattn_forward(lay: Layout, q, k, v, o, scale: float, rowbound, lse=None, fl
                                _ptr(lse), flags, _stream(stream))
     if raise_on_error:
         _check(st, "bsattn_forward")
+    return st
+
+
+def bsattn_forward_noalloc(q, k, v, o, B: int, H: int, L: int, D: int, block_size: int, block_mask,
+                           scale: float, rowbound, lse=None, flags: int = 0, stream=None,
+                           raise_on_error: bool = True) -> int:
+    """The forward without a layout, for callers that may not allocate device memory
+    (see bsattn_forward_noalloc in include/bsattn.h)."""
+    m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
+    st = load().bsattn_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, L, D, block_size, m.ctypes.data,
+                                       float(scale), _ptr(rowbound), _ptr(lse), flags, _stream(stream))
+    if raise_on_error:
+        _check(st, "bsattn_forward_noalloc")
     return st
 
 

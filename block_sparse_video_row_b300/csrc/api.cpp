@@ -208,6 +208,13 @@ bsattn_status check_runnable(const bsattn_layout_s *lay) {
 
 }  // namespace
 
+namespace bsv {
+bool encode_layout_maps(const bsattn_layout_s *lay, const void *q, const void *k, const void *v, CUtensorMap *tq,
+                        CUtensorMap *tk, CUtensorMap *tv) {
+    return encode_fn() && encode_q_map(tq, *lay, q) && encode_kv_map(tk, *lay, k) && encode_kv_map(tv, *lay, v);
+}
+}  // namespace bsv
+
 extern "C" {
 
 bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+struct bsattn_layout_s;
+
 namespace bsv {
 
 constexpr int kQTile = 128;           // query rows per tile (the MMA M dimension)
@@ -73,5 +75,11 @@ cudaError_t configure_attention_d128(int N);
 // Dynamic shared memory of one CTA for (D, N).
 size_t smem_attention_d64(int N);
 size_t smem_attention_d128(int N);
+
+// TMA tensor maps of Q (3-D, frame-local boxes) and K, V (2-D) for a layout's shape;
+// works for plan-only layouts too.  False if the driver entry point is missing or
+// the driver rejects a map.
+bool encode_layout_maps(const bsattn_layout_s *lay, const void *q, const void *k, const void *v, CUtensorMap *tq,
+                        CUtensorMap *tk, CUtensorMap *tv);
 
 }  // namespace bsv

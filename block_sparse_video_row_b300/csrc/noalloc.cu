@@ -1,0 +1,177 @@
+// bsattn_forward_noalloc: the attention forward for callers that may not allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc: a plugin whose host framework owns every
+// byte of device memory through its own fixed arena, or a streaming loop that
+// must not take cudaMalloc's implicit device synchronisation in the middle of a
+// chunk.  bsattn_create_layout allocates a few device buffers (the work plan and
+// the underflow-guard workspace), so such a caller cannot use bsattn_forward.
+// This entry point runs the same kernels with those buffers placed in one
+// fixed, file-scope device array instead.
+//
+// The array is kNoallocScratchBytes (1 MiB) of device memory that every GPU which
+// loads this library keeps until the process exits.  All calls share it and it
+// keeps the contents of the last call; each call rewrites what must start at
+// zero (status word, counters, per-unit flags) together with the plan.  Calls
+// whose work overlaps on the GPU (different streams, or different host threads
+// without ordering) race on the array.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "bsattn.h"
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = BSATTN_NOALLOC_SCRATCH_BYTES;
+
+// The scratch array.  In host code `g_scratch` names a host-side stand-in, not a
+// device address: its address must come from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool ready = false;
+    unsigned char *scratch = nullptr;  // device address of g_scratch on this device
+    int num_sms = 0;
+};
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Once per device, with that device current: check it, fetch the device address of
+// the scratch array and the SM count.
+bsattn_status device_setup(int dev, DeviceState **out) {
+    if (dev < 0 || dev >= kMaxDevices) return BSATTN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BSATTN_ERR_DEVICE;
+        if (major != 10 || minor != 3) return BSATTN_ERR_DEVICE;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return BSATTN_ERR_CUDA;
+        d.scratch = static_cast<unsigned char *>(p);
+        d.num_sms = sms;
+        d.ready = true;
+    }
+    *out = &d;
+    return BSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, const void *v, void *o, int32_t B,
+                                                int32_t H, int64_t L, int32_t D, int32_t block_size,
+                                                const uint8_t *block_mask, float scale, const float *rowbound,
+                                                float *lse, int32_t flags, bsattn_stream_t stream) {
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK)) != 0) return BSATTN_ERR_INVALID_ARG;
+    const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
+    if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
+    const auto mis16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) != 0; };
+    if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return BSATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(rowbound) & 3) || (reinterpret_cast<uintptr_t>(lse) & 3))
+        return BSATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+
+    // The work plan, built on the host only (the plan-only layout touches no device).
+    bsattn_layout_t plan = nullptr;
+    bsattn_status st = bsattn_create_layout(&plan, B, H, L, D, block_size, block_mask, BSATTN_PLAN_ONLY);
+    if (st != BSATTN_OK) return st;
+    bsattn_layout_info_t info;
+    bsattn_layout_info(plan, &info);
+    const size_t n = static_cast<size_t>(info.n_units);
+    const size_t nnz = static_cast<size_t>(info.nnz_blocks > 0 ? info.nnz_blocks : 1);
+
+    // Scratch layout: guard workspace (8 header ints: status, -, -, -, fallback count,
+    // fallback rows, -, -; then per-unit flags; then the fallback list), the work list,
+    // the allowed-block CSR.  Sizes beyond the array are rejected here, before any
+    // device work.
+    const size_t off_units = align256((8 + 2 * n) * 4);
+    const size_t off_rowptr = align256(off_units + 16 * n);
+    const size_t off_colidx = align256(off_rowptr + 4 * (static_cast<size_t>(info.nb) + 1));
+    const size_t total = off_colidx + 4 * nnz;
+    if (total > kNoallocScratchBytes) {
+        bsattn_destroy(plan);
+        return BSATTN_ERR_UNSUPPORTED;
+    }
+    std::vector<unsigned char> host(total, 0);
+    bsattn_layout_export(plan, reinterpret_cast<int32_t *>(host.data() + off_rowptr),
+                         reinterpret_cast<int32_t *>(host.data() + off_colidx),
+                         reinterpret_cast<int32_t *>(host.data() + off_units));
+
+    int dev = -1;
+    DeviceState *ds = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        bsattn_destroy(plan);
+        return BSATTN_ERR_DEVICE;
+    }
+    st = device_setup(dev, &ds);
+    if (st != BSATTN_OK) {
+        bsattn_destroy(plan);
+        return st;
+    }
+    CUtensorMap tq, tk, tv;
+    if (!bsv::encode_layout_maps(plan, q, k, v, &tq, &tk, &tv)) {
+        bsattn_destroy(plan);
+        return BSATTN_ERR_CUDA;
+    }
+    cudaError_t e = info.D == 128 ? bsv::configure_attention_d128(info.kv_tile)
+                                  : bsv::configure_attention_d64(info.kv_tile);
+    bsattn_destroy(plan);
+    if (e != cudaSuccess) return BSATTN_ERR_CUDA;
+
+    // One stream-ordered copy writes the plan and zeroes the workspace (the host
+    // buffer may be released on return: a pageable-source copy is staged first).
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *base = ds->scratch;
+    e = cudaMemcpyAsync(base, host.data(), total, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return BSATTN_ERR_CUDA;
+
+    int32_t *ws = reinterpret_cast<int32_t *>(base);
+    bsv::AttnParams p;
+    p.units = reinterpret_cast<const int4 *>(base + off_units);
+    p.n_units = info.n_units;
+    p.row_ptr = reinterpret_cast<const int32_t *>(base + off_rowptr);
+    p.col_idx = reinterpret_cast<const int32_t *>(base + off_colidx);
+    p.rowbound = rowbound;
+    p.o = static_cast<uint16_t *>(o);
+    p.lse = lse;
+    p.ws.status = ws + 0;
+    p.ws.fb_count = ws + 4;
+    p.ws.fb_rows = ws + 5;
+    p.ws.unit_flag = ws + 8;
+    p.ws.fb_list = ws + 8 + n;
+    p.L = L;
+    p.block = block_size;
+    p.nb = info.nb;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    uint64_t ms = 4000;
+    if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
+        const long long val = std::atoll(env);
+        if (val > 0) ms = static_cast<uint64_t>(val);
+    }
+    p.timeout_ns = ms * 1000000ull;
+    const int grid = std::max(1, std::min(info.n_units, ds->num_sms));
+    auto launch = [&](bool on) {
+        return info.D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, info.kv_tile, on, grid, s)
+                             : bsv::launch_attention_d64(tq, tk, tv, p, info.kv_tile, on, grid, s);
+    };
+    if (online) {
+        p.mode = bsv::kModeOnlineAll;
+        return launch(true) == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+    }
+    p.mode = bsv::kModeBound;
+    if (launch(false) != cudaSuccess) return BSATTN_ERR_CUDA;
+    if (flags & BSATTN_NO_FALLBACK) return BSATTN_OK;
+    p.mode = bsv::kModeFallback;
+    return launch(true) == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}

@@ -143,6 +143,42 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
                              float scale, const float *rowbound, float *lse, int32_t flags,
                              bsattn_stream_t stream);
 
+/*
+ * bsattn_forward_noalloc -- the forward of bsattn_forward for callers that may not
+ * allocate device memory.  The pages have no counterpart: this is a deployment
+ * convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc: a plugin whose host framework owns all
+ * device memory through its own fixed arena, or a streaming loop that must not
+ * take cudaMalloc's implicit device synchronisation between chunks.  Creating a
+ * layout allocates the work plan and the guard workspace on the device; this
+ * entry point needs no layout.  It builds the plan on the host for each call and
+ * keeps plan and workspace in one static device array of
+ * BSATTN_NOALLOC_SCRATCH_BYTES (1 MiB) inside the library, which every GPU that
+ * loads the library holds until the process exits.  It calls no allocating CUDA
+ * or library routine.
+ *   q, k, v, o, scale, rowbound, lse, flags: as for bsattn_forward (device pointers;
+ *             rowbound from bsattn_row_bounds or any equal bound).
+ *   B, H, L, D, block_size, block_mask: as for bsattn_create_layout (mask on the host).
+ * Limits: the plan (work units x 24 bytes + the allowed-block table, each part
+ * rounded up to 256 bytes) must fit in the array, about 40,000 work units (the
+ * 720p chunk uses 4,680, the 1080p chunk 9,984); a larger problem returns
+ * BSATTN_ERR_UNSUPPORTED before any device work.
+ * The first call on a device (with that device current) looks up the array's
+ * device address; make that first call before any stream capture.  Each call
+ * copies the plan and zeroed guard counters into the array with one
+ * cudaMemcpyAsync from host memory on `stream`, so the call may wait for work
+ * already queued on that stream.  All calls share the array and it keeps the
+ * last call's contents: calls whose GPU work overlaps (other streams, other
+ * host threads) race.  Statistics are not kept (bsattn_query_stats needs a layout).
+ * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA or DEVICE.
+ */
+#define BSATTN_NOALLOC_SCRATCH_BYTES (1 << 20)
+bsattn_status bsattn_forward_noalloc(const void *q, const void *k, const void *v, void *o, int32_t B, int32_t H,
+                                     int64_t L, int32_t D, int32_t block_size, const uint8_t *block_mask,
+                                     float scale, const float *rowbound, float *lse, int32_t flags,
+                                     bsattn_stream_t stream);
+
 /* Free the layout's device buffers and host plan.  NULL is ignored. */
 void bsattn_destroy(bsattn_layout_t lay);
 

@@ -1,0 +1,92 @@
+"""bsattn_forward_noalloc: the forward for callers that may not allocate device memory.
+
+A plugin whose host framework owns all device memory, or a streaming loop that
+cannot take cudaMalloc's implicit synchronisation, cannot create a layout (that
+allocates the work plan and the guard workspace on the device).  The no-alloc
+entry point keeps those in a fixed device array inside the library.  Here it is
+called through the C ABI twice in a row and each output is compared with the
+layout-based bsattn_forward on the same inputs, with the tolerance of the other
+GPU tests.  The first call uses inputs whose bound is too loose for some rows,
+so the guard fills the fallback list in the shared array; the second call must
+start from cleared counters and flags.  This file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+
+from block_sparse_video_row_b300 import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module")
+def ba():
+    from block_sparse_video_row_b300 import _build, bsattn
+    _build.build()
+    bsattn.load()
+    return bsattn
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _f64(t):
+    return synth.bf16_bits_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def _case(name, loose_key=False):
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.make_qkv(w)
+    if loose_key:  # one key 1e4 times longer: the bound underflows for the rows that read it
+        k = k.copy()
+        k[0, 0, 3] = synth.f32_to_bf16_bits((synth.bf16_bits_to_f64(k[0, 0, 3]) * 1e4).astype(np.float32))
+    return w, q, k, v
+
+
+def _both(ba, w, q, k, v):
+    mask = w.block_mask()
+    dq, dk, dv = _dev(q), _dev(k), _dev(v)
+    lay = ba.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask)
+    qn = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device="cuda")
+    km = torch.empty((w.B, w.H, w.nb), dtype=torch.float32, device="cuda")
+    rb = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device="cuda")
+    ba.bsattn_row_bounds(lay, dq, dk, w.scale, qn, km, rb)
+    o_ref = torch.full_like(dq, float("nan"))
+    ba.bsattn_forward(lay, dq, dk, dv, o_ref, w.scale, rb, None, ba.BSATTN_BOUND)
+    fb_rows, _, status = ba.bsattn_query_stats(lay)
+    assert status == 0
+    o_na = torch.full_like(dq, float("nan"))
+    ba.bsattn_forward_noalloc(dq, dk, dv, o_na, w.B, w.H, w.L, w.D, w.block, mask, w.scale, rb, None,
+                              ba.BSATTN_BOUND)
+    torch.cuda.synchronize()
+    lay.destroy()
+    return _f64(o_ref), _f64(o_na), fb_rows
+
+
+def test_noalloc_matches_forward_on_two_calls_in_a_row(ba):
+    # call 1: rows that need the online-max rerun (fallback list in the shared array)
+    w, q, k, v = _case("tiny", loose_key=True)
+    ref, got, fb_rows = _both(ba, w, q, k, v)
+    assert fb_rows > 0
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)) and err.max() <= O_MAX and err.mean() <= O_MEAN
+    # call 2: a larger problem, nothing to rerun; counters and flags must start from zero
+    w, q, k, v = _case("small")
+    ref, got, fb_rows = _both(ba, w, q, k, v)
+    assert fb_rows == 0
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)) and err.max() <= O_MAX and err.mean() <= O_MEAN
+
+
+def test_noalloc_rejects_plans_beyond_its_array(ba):
+    # 512 heads of the 720p shape: ~100k work units, more than the 1 MiB array holds.
+    # The check comes before any device work, so the pointers are never dereferenced.
+    fake = 1 << 20
+    mask = synth.window_mask(13, 1, True)
+    st = ba.bsattn_forward_noalloc(fake, fake, fake, fake, 1, 512, 13 * 3600, 128, 3600, mask, 0.088, fake, None,
+                                   0, raise_on_error=False)
+    assert st == ba.BSATTN_ERR_UNSUPPORTED
