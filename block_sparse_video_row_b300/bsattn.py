@@ -42,7 +42,7 @@ EXPORTED = ("bsattn_create_layout", "bsattn_row_bounds", "bsattn_forward", "bsat
 class LayoutInfo(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("nb", ctypes.c_int32), ("L", ctypes.c_int64),
-                ("nnz_blocks", ctypes.c_int32), ("kv_tile", ctypes.c_int32),
+                ("nnz_blocks", ctypes.c_int32), ("kv_tile", ctypes.c_int32), ("key_tiles", ctypes.c_int32),
                 ("q_tiles_per_block", ctypes.c_int32), ("n_units", ctypes.c_int32),
                 ("mma_rows", ctypes.c_int64), ("useful_flop", ctypes.c_double)]
 
@@ -86,7 +86,7 @@ def load(path: Optional[str] = None):
     lib.bsattn_forward_noalloc.restype = i32
     lib.bsattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, i32, vp, f32, vp, vp, i32, vp]
     lib.bsattn_layout_export.restype = i32
-    lib.bsattn_layout_export.argtypes = [vp, vp, vp, vp]
+    lib.bsattn_layout_export.argtypes = [vp, vp, vp, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -217,15 +217,21 @@ def bsattn_layout_info(lay: Layout) -> LayoutInfo:
     return info
 
 
-def bsattn_layout_export(lay: Layout):
-    """(row_ptr [nb+1], col_idx [nnz], units [n_units, 4]) as int32 numpy arrays."""
+def bsattn_layout_export(lay: Layout, with_tiles: bool = False):
+    """(row_ptr [nb+1], col_idx [nnz], units [n_units, 4]) as int32 numpy arrays; with_tiles adds
+    (tile_ptr [nb+1], tiles [key_tiles, 2])."""
     i = lay.info
     row_ptr = np.zeros(i.nb + 1, np.int32)
     col_idx = np.zeros(max(i.nnz_blocks, 1), np.int32)
     units = np.zeros((i.n_units, 4), np.int32)
-    _check(load().bsattn_layout_export(lay.handle, row_ptr.ctypes.data, col_idx.ctypes.data, units.ctypes.data),
-           "bsattn_layout_export")
-    return row_ptr, col_idx[:i.nnz_blocks].copy(), units
+    tile_ptr = np.zeros(i.nb + 1, np.int32)
+    tiles = np.zeros((max(i.key_tiles, 1), 2), np.int32)
+    _check(load().bsattn_layout_export(lay.handle, row_ptr.ctypes.data, col_idx.ctypes.data, units.ctypes.data,
+                                       tile_ptr.ctypes.data, tiles.ctypes.data), "bsattn_layout_export")
+    out = (row_ptr, col_idx[:i.nnz_blocks].copy(), units)
+    if with_tiles:
+        out += (tile_ptr, tiles[:i.key_tiles].copy())
+    return out
 
 
 # ------------------------------------------------------------------------------------------------

@@ -19,11 +19,13 @@ struct bsattn_layout_s {
     int64_t L = 0;
     bool plan_only = false;
     std::vector<int32_t> row_ptr, col_idx, units;
+    std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs
     int32_t kv_tile = 0, qt_per_block = 0, n_units = 0;
     int64_t mma_rows = 0;
     double useful_flop = 0.0;
     int device = -1, num_sms = 0;
-    int32_t *d_row_ptr = nullptr, *d_col_idx = nullptr;
+    int32_t *d_row_ptr = nullptr, *d_col_idx = nullptr, *d_tile_ptr = nullptr;
+    int2 *d_tiles = nullptr;
     int4 *d_units = nullptr;
     int32_t *d_ws = nullptr;
     bsv::Workspace ws{};
@@ -41,14 +43,6 @@ bsattn_status from_cuda(cudaError_t e) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Key tile: the largest multiple of 16 that divides the frame block, at most 128
-// (a tile must never straddle a frame edge: no element mask on the key side).
-int32_t choose_kv_tile(int32_t bs) {
-    for (int32_t n = bsv::kMaxKvTile; n >= 16; n -= 16)
-        if (bs % n == 0) return n;
-    return 16;
-}
-
 void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     const int32_t nb = lay.nb;
     lay.row_ptr.assign(static_cast<size_t>(nb) + 1, 0);
@@ -58,9 +52,31 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
             if (mask[static_cast<int64_t>(qb) * nb + kb]) lay.col_idx.push_back(kb);
         lay.row_ptr[qb + 1] = static_cast<int32_t>(lay.col_idx.size());
     }
-    lay.kv_tile = choose_kv_tile(lay.bs);
+    // Key tiles: the allowed key blocks of a query block, grouped into runs of
+    // consecutive frames (contiguous keys, all allowed), each run cut into tiles of
+    // kKvTile keys and one last tile of the remaining keys.  Frames are multiples of
+    // 16 tokens, so every width is a multiple of 16: an exactly sized MMA, with no
+    // element mask and no padding, and no tile reaches into a masked frame.
+    lay.kv_tile = bsv::kKvTile;
     lay.qt_per_block = (lay.bs + bsv::kQTile - 1) / bsv::kQTile;
-    const int32_t tpb = lay.bs / lay.kv_tile;
+    lay.tile_ptr.assign(static_cast<size_t>(nb) + 1, 0);
+    lay.tiles.clear();
+    for (int32_t qb = 0; qb < nb; ++qb) {
+        int32_t e = lay.row_ptr[qb];
+        const int32_t e1 = lay.row_ptr[qb + 1];
+        while (e < e1) {
+            int32_t run_end = e + 1;
+            while (run_end < e1 && lay.col_idx[run_end] == lay.col_idx[run_end - 1] + 1) ++run_end;
+            const int64_t k0 = static_cast<int64_t>(lay.col_idx[e]) * lay.bs;
+            const int64_t k1 = static_cast<int64_t>(lay.col_idx[run_end - 1] + 1) * lay.bs;
+            for (int64_t k = k0; k < k1; k += bsv::kKvTile) {
+                lay.tiles.push_back(static_cast<int32_t>(k));
+                lay.tiles.push_back(static_cast<int32_t>(std::min<int64_t>(bsv::kKvTile, k1 - k)));
+            }
+            e = run_end;
+        }
+        lay.tile_ptr[qb + 1] = static_cast<int32_t>(lay.tiles.size() / 2);
+    }
 
     struct Unit {
         int32_t bh, qb, qt0, nt;
@@ -71,10 +87,12 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     us.reserve(static_cast<size_t>(BH) * nb * ((lay.qt_per_block + 1) / 2));
     for (int32_t bh = 0; bh < BH; ++bh)
         for (int32_t qb = 0; qb < nb; ++qb) {
-            const int64_t nkv = static_cast<int64_t>(lay.row_ptr[qb + 1] - lay.row_ptr[qb]) * tpb;
+            const int64_t keys = static_cast<int64_t>(lay.row_ptr[qb + 1] - lay.row_ptr[qb]) * lay.bs;
+            const int64_t ntile = lay.tile_ptr[qb + 1] - lay.tile_ptr[qb];
             for (int32_t qt0 = 0; qt0 < lay.qt_per_block; qt0 += 2) {
                 const int32_t nt = std::min(2, lay.qt_per_block - qt0);
-                us.push_back({bh, qb, qt0, nt, nkv * nt});
+                // cost ~ MMA work (keys) plus a per-tile pipeline overhead
+                us.push_back({bh, qb, qt0, nt, (keys + 32 * ntile) * nt});
             }
         }
     // Largest first (longest-processing-time order for the persistent CTAs); equal
@@ -128,7 +146,8 @@ bool encode_q_map(CUtensorMap *m, const bsattn_layout_s &lay, const void *ptr) {
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// K and V viewed as [B*H*L rows][D]; boxes of kv_tile rows never leave a frame.
+// K and V viewed as [B*H*L rows][D].  A box of kv_tile rows starts at a key tile; when the
+// tile is the narrower last one of a run, the rows past it are loaded but never used.
 bool encode_kv_map(CUtensorMap *m, const bsattn_layout_s &lay, const void *ptr) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lay.D),
                                 static_cast<cuuint64_t>(lay.B) * lay.H * static_cast<cuuint64_t>(lay.L)};
@@ -144,8 +163,11 @@ void free_device(bsattn_layout_s *lay) {
     if (lay->d_row_ptr) cudaFree(lay->d_row_ptr);
     if (lay->d_col_idx) cudaFree(lay->d_col_idx);
     if (lay->d_units) cudaFree(lay->d_units);
+    if (lay->d_tile_ptr) cudaFree(lay->d_tile_ptr);
+    if (lay->d_tiles) cudaFree(lay->d_tiles);
     if (lay->d_ws) cudaFree(lay->d_ws);
-    lay->d_row_ptr = lay->d_col_idx = nullptr;
+    lay->d_row_ptr = lay->d_col_idx = lay->d_tile_ptr = nullptr;
+    lay->d_tiles = nullptr;
     lay->d_units = nullptr;
     lay->d_ws = nullptr;
 }
@@ -160,14 +182,16 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
     lay.device = dev;
     lay.num_sms = prop.multiProcessorCount;
 
-    cudaError_t e = lay.D == 128 ? bsv::configure_attention_d128(lay.kv_tile)
-                                 : bsv::configure_attention_d64(lay.kv_tile);
+    cudaError_t e = lay.D == 128 ? bsv::configure_attention_d128() : bsv::configure_attention_d64();
     if (e != cudaSuccess) return from_cuda(e);
 
     const size_t nnz = std::max<size_t>(lay.col_idx.size(), 1);
+    const size_t ntiles = std::max<size_t>(lay.tiles.size() / 2, 1);
     const size_t ws_ints = kWsHeader + 2 * static_cast<size_t>(lay.n_units);
     if ((e = cudaMalloc(&lay.d_row_ptr, lay.row_ptr.size() * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_col_idx, nnz * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&lay.d_tile_ptr, lay.tile_ptr.size() * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&lay.d_tiles, ntiles * sizeof(int2))) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_units, static_cast<size_t>(lay.n_units) * sizeof(int4))) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_ws, ws_ints * 4)) != cudaSuccess) {
         free_device(&lay);
@@ -180,6 +204,11 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
              cudaSuccess) ||
         (e = cudaMemcpy(lay.d_units, lay.units.data(), lay.units.size() * 4, cudaMemcpyHostToDevice)) !=
             cudaSuccess ||
+        (e = cudaMemcpy(lay.d_tile_ptr, lay.tile_ptr.data(), lay.tile_ptr.size() * 4, cudaMemcpyHostToDevice)) !=
+            cudaSuccess ||
+        (!lay.tiles.empty() &&
+         (e = cudaMemcpy(lay.d_tiles, lay.tiles.data(), lay.tiles.size() * 4, cudaMemcpyHostToDevice)) !=
+             cudaSuccess) ||
         (e = cudaMemset(lay.d_ws, 0, ws_ints * 4)) != cudaSuccess) {
         free_device(&lay);
         return from_cuda(e);
@@ -309,8 +338,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     bsv::AttnParams p;
     p.units = lay->d_units;
     p.n_units = lay->n_units;
-    p.row_ptr = lay->d_row_ptr;
-    p.col_idx = lay->d_col_idx;
+    p.tile_ptr = lay->d_tile_ptr;
+    p.tiles = lay->d_tiles;
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
@@ -322,8 +351,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.timeout_ns = lay->timeout_ns;
     const int grid = std::max(1, std::min(lay->n_units, lay->num_sms));
     auto launch = [&](bool on) {
-        return lay->D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, lay->kv_tile, on, grid, s)
-                             : bsv::launch_attention_d64(tq, tk, tv, p, lay->kv_tile, on, grid, s);
+        return lay->D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, on, grid, s)
+                             : bsv::launch_attention_d64(tq, tk, tv, p, on, grid, s);
     };
     if (online) {
         p.mode = bsv::kModeOnlineAll;
@@ -388,6 +417,7 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
     info->L = lay->L;
     info->nnz_blocks = static_cast<int32_t>(lay->col_idx.size());
     info->kv_tile = lay->kv_tile;
+    info->key_tiles = static_cast<int32_t>(lay->tiles.size() / 2);
     info->q_tiles_per_block = lay->qt_per_block;
     info->n_units = lay->n_units;
     info->mma_rows = lay->mma_rows;
@@ -395,8 +425,11 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
     return BSATTN_OK;
 }
 
-bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units) {
+bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units,
+                                   int32_t *tile_ptr, int32_t *tiles) {
     if (!lay) return BSATTN_ERR_INVALID_ARG;
+    if (tile_ptr) std::memcpy(tile_ptr, lay->tile_ptr.data(), lay->tile_ptr.size() * 4);
+    if (tiles && !lay->tiles.empty()) std::memcpy(tiles, lay->tiles.data(), lay->tiles.size() * 4);
     if (row_ptr) std::memcpy(row_ptr, lay->row_ptr.data(), lay->row_ptr.size() * 4);
     if (col_idx && !lay->col_idx.empty()) std::memcpy(col_idx, lay->col_idx.data(), lay->col_idx.size() * 4);
     if (units && !lay->units.empty()) std::memcpy(units, lay->units.data(), lay->units.size() * 4);

@@ -4,23 +4,25 @@
 // The method ("HeyGen Avatar IV on Trillium TPU" deep-dive, sections
 // 把 block 縮到 16 and 拿掉 softmax 的序列相依; "How is HeyGen optimizing AI video
 // on Google Cloud TPUs", section "Innovating Beyond Serial Dependencies"):
-//   * query and key blocks are whole frames; the mask says which key frames a
-//     query frame reads.  Key tiles are N keys with N a multiple of 16 that
-//     divides the frame, so a tile never crosses a frame edge and no element
-//     mask, tail pass or padding exists on the key side;
+//   * query and key blocks are whole frames, a multiple of 16 tokens; the mask
+//     says which key frames a query frame reads.  The allowed frames of a query
+//     frame form runs of consecutive frames; each run is cut into key tiles of
+//     128 keys plus one last tile of the remaining keys, itself a multiple of
+//     16, so every tile is an exactly sized MMA (N = its width): no element
+//     mask, no padding, and no tile reaches into a masked frame;
 //   * the softmax shift of row i is its Cauchy-Schwarz bound m_i (precomputed),
 //     so P = exp(scale*S - m_i) needs no running max and no rescaling of the
 //     accumulator: every key tile is independent.
 //
 // One CTA per SM processes work units: a unit is one or two 128-row query tiles
-// of the same frame (they share every K/V tile), looping over the unit's
-// allowed key tiles.
-//   warp 0     TMA producer: Q tiles, then a K ring and a V ring of STAGES tiles.
+// of the same frame (they share every K/V tile), looping over the frame's key
+// tiles.
+//   warp 0     TMA producer: Q tiles, then a ring of STAGES K and V tiles.
 //   warp 1     MMA issuer (one thread): S_t = Q_t K^T (A, B from smem) and
 //              O_t += P_t V (A = P_t from TMEM, B = V from smem), t = 0, 1.
 //   warps 4-7  softmax of query tile 0; warps 8-11 of tile 1 (one row per thread).
 // TMEM (512 columns): S_0/P_0 at column 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
-// P_t (bf16, two per 32-bit column) overwrites the first N/2 columns of S_t.
+// P_t (bf16, two per 32-bit column) overwrites the first w/2 columns of S_t.
 //
 // Per key tile the MMA thread issues, in order, PV_0(j), S_0(j+1), PV_1(j),
 // S_1(j+1): while softmax 0 works on S_0 the tensor cores run tile 1's MMAs and
@@ -38,10 +40,10 @@
 
 namespace bsv {
 
-template <int D, int N>
+template <int D>
 struct AttnCfg {
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(N % 16 == 0 && N >= 16 && N <= kMaxKvTile, "key tile");
+    static constexpr int N = kKvTile;                 // keys per full tile
     static constexpr int DH = D / 64;                 // 64-column (128-byte) halves of a row
     static constexpr int HALF_Q = kQTile * 128;       // bytes of one half of a Q tile
     static constexpr int Q_TILE = DH * HALF_Q;
@@ -60,7 +62,8 @@ struct AttnCfg {
     // Above half of the SM's shared memory, so one CTA (and one TMEM owner) per SM.
     static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
-    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kQTile, N, false, false);
+    // QK^T descriptor without its N field (set per tile from the tile's width).
+    static constexpr uint32_t IDESC_QK0 = idesc_bf16_f32(kQTile, 16, false, false) & ~(0x3Fu << 17);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kQTile, D, false, true);
 };
 
@@ -103,63 +106,89 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint6
     }
 }
 
+// All 384 threads of the CTA (each warp converged) meet here.
+__device__ __forceinline__ void cta_barrier() {
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;" ::"n"(kAttnThreads) : "memory");
+}
+
 // ----------------------------------------------------------------------------------------------
 // softmax of one S tile (one row per thread), P written back to TMEM as bf16
 
-// Bound softmax: P = 2^(S*c1 - m2), c1 = scale*log2(e), m2 = m_i*log2(e).
-template <int N>
-__device__ __forceinline__ void softmax_tile_bound(uint32_t tS, float c1, float m2, float &l0, float &l1) {
-    constexpr int NC = N / 16;
+// Two logits -> two probabilities: P = 2^(S*c1 - m2) with c1 = scale*log2(e) and
+// m2 = the row shift in log2 units; returns them as packed bf16 and adds the
+// rounded values (the ones the P.V product uses) to the pair accumulator l2.
+__device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint64_t c1x2, uint64_t nm2x2,
+                                                 uint64_t &l2) {
+    float x0, x1;
+    f2_split(f2_fma(f2_from_bits(s0, s1), c1x2, nm2x2), x0, x1);
+    const uint32_t pk = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+    l2 = f2_add(l2, f2_from_bits(pk << 16, pk & 0xFFFF0000u));
+    return pk;
+}
+
+// One S tile of w columns (a multiple of 16, <= 128): TMEM loads of 32 columns are
+// double-buffered so the load of group g+1 overlaps the arithmetic of group g.
+// P of group g (16 packed columns) overwrites S columns [16g, 16g+16), all of
+// which were loaded by then; the load in flight reads columns >= 32(g+1).
+__device__ __forceinline__ void softmax_tile(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, uint64_t &la,
+                                             uint64_t &lb) {
+    uint32_t buf[2][32];
+    if (w >= 32)
+        tmem_ld32(tS, buf[0]);
+    else
+        tmem_ld16_into32(tS, buf[0]);
 #pragma unroll
-    for (int c = 0; c < NC; c += 2) {
-        uint32_t a[16], b[16];
-        tmem_ld16(tS + c * 16, a);
-        if (c + 1 < NC) tmem_ld16(tS + (c + 1) * 16, b);
-        tmem_wait_ld();
-        reg_fence16(a);
-        if (c + 1 < NC) reg_fence16(b);
-        uint32_t pa[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float x0 = ex2_approx(fmaf(__uint_as_float(a[2 * e]), c1, -m2));
-            const float x1 = ex2_approx(fmaf(__uint_as_float(a[2 * e + 1]), c1, -m2));
-            pa[e] = pack_bf16x2(x0, x1);
-            l0 += bf16lo_f32(pa[e]);
-            l1 += bf16hi_f32(pa[e]);
-        }
-        tmem_st8(tS + c * 8, pa);
-        if (c + 1 < NC) {
-            uint32_t pb[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float x0 = ex2_approx(fmaf(__uint_as_float(b[2 * e]), c1, -m2));
-                const float x1 = ex2_approx(fmaf(__uint_as_float(b[2 * e + 1]), c1, -m2));
-                pb[e] = pack_bf16x2(x0, x1);
-                l0 += bf16lo_f32(pb[e]);
-                l1 += bf16hi_f32(pb[e]);
+    for (int g = 0; g < kKvTile / 32; ++g) {
+        if (32 * g < w) {
+            const bool full = w - 32 * g >= 32;
+            tmem_wait_ld();
+            reg_fence32(buf[g & 1]);
+            if (32 * (g + 1) < w) {
+                if (w - 32 * (g + 1) >= 32)
+                    tmem_ld32(tS + 32 * (g + 1), buf[(g + 1) & 1]);
+                else
+                    tmem_ld16_into32(tS + 32 * (g + 1), buf[(g + 1) & 1]);
             }
-            tmem_st8(tS + (c + 1) * 8, pb);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                pk[e] = softmax_pair(buf[g & 1][2 * e], buf[g & 1][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
+            if (full) {
+#pragma unroll
+                for (int e = 8; e < 16; ++e)
+                    pk[e] = softmax_pair(buf[g & 1][2 * e], buf[g & 1][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
+                tmem_st16(tS + 16 * g, pk);
+            } else {
+                uint32_t h[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) h[e] = pk[e];
+                tmem_st8(tS + 16 * g, h);
+            }
         }
     }
 }
 
-template <int N>
-__device__ __forceinline__ float tile_row_max(uint32_t tS) {
-    constexpr int NC = N / 16;
+// Row max of one S tile (raw logits), for the online-max variant.
+__device__ __forceinline__ float tile_row_max(uint32_t tS, int w) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < NC; c += 2) {
-        uint32_t a[16], b[16];
-        tmem_ld16(tS + c * 16, a);
-        if (c + 1 < NC) tmem_ld16(tS + (c + 1) * 16, b);
-        tmem_wait_ld();
-        reg_fence16(a);
-        if (c + 1 < NC) reg_fence16(b);
+    for (int g = 0; g < kKvTile / 32; ++g) {
+        if (32 * g < w) {
+            uint32_t a[32];
+            const bool full = w - 32 * g >= 32;
+            if (full)
+                tmem_ld32(tS + 32 * g, a);
+            else
+                tmem_ld16_into32(tS + 32 * g, a);
+            tmem_wait_ld();
+            reg_fence32(a);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
-        if (c + 1 < NC) {
+            for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
+            if (full) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(b[e]));
+                for (int e = 16; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
+            }
         }
     }
     return mx;
@@ -168,26 +197,37 @@ __device__ __forceinline__ float tile_row_max(uint32_t tS) {
 // Multiply one row of the O accumulator (D fp32 columns) by alpha (warp-collective).
 template <int D>
 __device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
+    const uint64_t a2 = f2_make(alpha, alpha);
 #pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-        uint32_t a[16];
-        tmem_ld16(tO + c * 16, a);
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tO + c * 32, a);
         tmem_wait_ld();
-        reg_fence16(a);
+        reg_fence32(a);
+        uint32_t r0[16], r1[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) * alpha);
-        tmem_st16(tO + c * 16, a);
+        for (int e = 0; e < 8; ++e) {
+            float x0, x1;
+            f2_split(f2_mul(f2_from_bits(a[2 * e], a[2 * e + 1]), a2), x0, x1);
+            r0[2 * e] = __float_as_uint(x0);
+            r0[2 * e + 1] = __float_as_uint(x1);
+            f2_split(f2_mul(f2_from_bits(a[16 + 2 * e], a[16 + 2 * e + 1]), a2), x0, x1);
+            r1[2 * e] = __float_as_uint(x0);
+            r1[2 * e + 1] = __float_as_uint(x1);
+        }
+        tmem_st16(tO + c * 32, r0);
+        tmem_st16(tO + c * 32 + 16, r1);
     }
     tmem_wait_st();
 }
 
 // ----------------------------------------------------------------------------------------------
 
-template <int D, int N, bool ONLINE>
+template <int D, bool ONLINE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-    using C = AttnCfg<D, N>;
+    using C = AttnCfg<D>;
     const int n_seq = p.mode == kModeFallback ? *reinterpret_cast<volatile int32_t *>(p.ws.fb_count) : p.n_units;
     if (static_cast<int>(blockIdx.x) >= n_seq) return;  // nothing to do: exit before any TMEM allocation
 
@@ -195,7 +235,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars bar = carve_bars<C::STAGES>(smem + C::OFF_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tpb = p.block / N;  // key tiles per frame block
 
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -228,27 +267,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     int *status = p.ws.status;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
+    // Registers move from the TMA/MMA warpgroup to the two softmax warpgroups.  The
+    // CTA launches with kLaunchRegs per thread (checked on the host before any launch)
+    // and 128 * kRegsLow + 256 * kRegsHigh <= 384 * kLaunchRegs.  Each role keeps its
+    // own branch to the end, where all threads meet at a named barrier.
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_kv = policy_evict_last();
             const uint64_t pol_q = policy_evict_first();
-            uint32_t q_uses[2] = {0, 0};
-            uint32_t g = 0;        // key tiles started by this CTA
+            uint32_t q_uses0 = 0, q_uses1 = 0;
+            uint32_t g = 0;           // key tiles started by this CTA
             uint32_t gk = 0, gv = 0;  // K / V copies issued
             bool ok = true;
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 const int4 U = p.units[unit_index(p, i)];
-                const int e0 = p.row_ptr[U.y], e1 = p.row_ptr[U.y + 1];
-                const int nkv = (e1 - e0) * tpb;
+                const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
                 if (nkv == 0) continue;
                 for (int t = 0; t < U.w && ok; ++t) {
-                    ok = mbar_wait(bar.q_empty + t, (q_uses[t] & 1) ^ 1, bar.abort, status, kStatusTimeout, tmo);
+                    uint32_t &qu = t ? q_uses1 : q_uses0;
+                    ok = mbar_wait(bar.q_empty + t, (qu & 1) ^ 1, bar.abort, status, kStatusTimeout, tmo);
                     if (!ok) break;
-                    ++q_uses[t];
+                    ++qu;
                     mbar_arrive_expect_tx(bar.q_full + t, C::Q_TILE);
 #pragma unroll
                     for (int h = 0; h < C::DH; ++h)
@@ -256,10 +300,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                     (U.z + t) * kQTile, U.x * p.nb + U.y, bar.q_full + t, pol_q);
                 }
                 for (int j = 0; j < nkv && ok; ++j, ++g) {
-                    const int kb = p.col_idx[e0 + j / tpb];
-                    const int row = static_cast<int>(static_cast<int64_t>(U.x) * p.L +
-                                                     static_cast<int64_t>(kb) * p.block) +
-                                    (j % tpb) * N;
+                    const int row = static_cast<int>(static_cast<int64_t>(U.x) * p.L) + p.tiles[t0 + j].x;
                     const int s = static_cast<int>(g % C::STAGES);
                     const uint32_t ph = (g / C::STAGES) & 1;
                     ok = mbar_wait(bar.k_empty + s, ph ^ 1, bar.abort, status, kStatusTimeout, tmo);
@@ -282,62 +323,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (!ok) {
                 // Let every copy already issued land before the CTA's shared memory goes away.
-                for (int t = 0; t < 2; ++t)
-                    if (q_uses[t]) mbar_drain(bar.q_full + t, (q_uses[t] - 1) & 1, tmo);
+                if (q_uses0) mbar_drain(bar.q_full + 0, (q_uses0 - 1) & 1, tmo);
+                if (q_uses1) mbar_drain(bar.q_full + 1, (q_uses1 - 1) & 1, tmo);
                 for (uint32_t x = (gk > C::STAGES ? gk - C::STAGES : 0); x < gk; ++x)
                     mbar_drain(bar.k_full + x % C::STAGES, (x / C::STAGES) & 1, tmo);
                 for (uint32_t x = (gv > C::STAGES ? gv - C::STAGES : 0); x < gv; ++x)
                     mbar_drain(bar.v_full + x % C::STAGES, (x / C::STAGES) & 1, tmo);
             }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
             const uint32_t q_base = smem_u32(smem + C::OFF_Q);
             const uint32_t k_base = smem_u32(smem + C::OFF_K);
             const uint32_t v_base = smem_u32(smem + C::OFF_V);
-            auto issue_qk = [&](int t, int s) {
+            // S_t = Q_t K^T over the first w keys of the stage (N = w in the instruction).
+            auto issue_qk = [&](int t, int s, int w) {
                 const uint32_t qa = q_base + t * C::Q_TILE;
                 const uint32_t ka = k_base + s * C::KV_TILE;
                 const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
+                const uint32_t idesc = C::IDESC_QK0 | (static_cast<uint32_t>(w >> 3) << 17);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
                     const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * C::HALF_Q + off, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * C::HALF_KV + off, 16, 1024);
-                    mma_ss(d, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int t, int s, bool acc) {
+            // O_t += P_t V over the first w keys (K = w, in steps of 16).
+            auto issue_pv = [&](int t, int s, int w, bool acc) {
                 const uint32_t va = v_base + s * C::KV_TILE;
                 const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
                 const uint32_t a = tmem + (t ? C::COL_S1 : C::COL_S0);
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(va + kk * 16 * 128, C::HALF_KV, 1024);
-                    mma_ts(d, a + kk * 8, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                    if (16 * kk < w) {
+                        const uint64_t bd = smem_desc_sw128(va + kk * 16 * 128, C::HALF_KV, 1024);
+                        mma_ts(d, a + kk * 8, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                    }
                 }
             };
-            uint32_t q_uses[2] = {0, 0}, p_uses[2] = {0, 0};
+            uint32_t q_uses0 = 0, q_uses1 = 0, p_uses0 = 0, p_uses1 = 0;
             uint32_t g = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 const int4 U = p.units[unit_index(p, i)];
-                const int nkv = (p.row_ptr[U.y + 1] - p.row_ptr[U.y]) * tpb;
+                const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
                 if (nkv == 0) continue;
                 const int nt = U.w;
-                for (int t = 0; t < nt && ok; ++t) {
-                    ok = mbar_wait(bar.q_full + t, q_uses[t] & 1, bar.abort, status, kStatusTimeout, tmo);
-                    ++q_uses[t];
+                ok = mbar_wait(bar.q_full + 0, q_uses0 & 1, bar.abort, status, kStatusTimeout, tmo);
+                ++q_uses0;
+                if (ok && nt > 1) {
+                    ok = mbar_wait(bar.q_full + 1, q_uses1 & 1, bar.abort, status, kStatusTimeout, tmo);
+                    ++q_uses1;
                 }
                 if (!ok) break;
+                int w_next = p.tiles[t0].y;
                 {
                     const int s0 = static_cast<int>(g % C::STAGES);
                     ok = mbar_wait(bar.k_full + s0, (g / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
                     if (!ok) break;
                     tc_fence_after();
                     for (int t = 0; t < nt; ++t) {
-                        issue_qk(t, s0);
+                        issue_qk(t, s0, w_next);
                         mma_commit(bar.s_full + t);
                         if (nkv == 1) mma_commit(bar.q_empty + t);
                     }
@@ -347,18 +394,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t gj = g + j, gn = g + j + 1;
                     const int sj = static_cast<int>(gj % C::STAGES), sn = static_cast<int>(gn % C::STAGES);
                     const bool more = j + 1 < nkv;
+                    const int wj = w_next;
+                    if (more) w_next = p.tiles[t0 + j + 1].y;
                     ok = mbar_wait(bar.v_full + sj, (gj / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
                     if (ok && more)
                         ok = mbar_wait(bar.k_full + sn, (gn / C::STAGES) & 1, bar.abort, status, kStatusTimeout,
                                        tmo);
                     for (int t = 0; t < nt && ok; ++t) {
-                        ok = mbar_wait(bar.p_full + t, p_uses[t] & 1, bar.abort, status, kStatusTimeout, tmo);
+                        uint32_t &pu = t ? p_uses1 : p_uses0;
+                        ok = mbar_wait(bar.p_full + t, pu & 1, bar.abort, status, kStatusTimeout, tmo);
                         if (!ok) break;
-                        ++p_uses[t];
+                        ++pu;
                         tc_fence_after();
-                        issue_pv(t, sj, j > 0);
+                        issue_pv(t, sj, wj, j > 0);
                         if (more) {
-                            issue_qk(t, sn);
+                            issue_qk(t, sn, w_next);
                             mma_commit(bar.s_full + t);
                             if (j + 2 == nkv) mma_commit(bar.q_empty + t);
                         } else {
@@ -375,7 +425,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mma_commit(bar.drain);
             mbar_drain(bar.drain, 0, tmo);
         }
-    } else if (warp >= 4) {
+        tc_fence_before();
+        cta_barrier();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ---------------------------------------------------------------- softmax + epilogue
         const int t = (warp - 4) >> 2;
         const int wq = warp & 3;
@@ -384,13 +441,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
         const float c1 = p.scale_log2;
+        const uint64_t c1x2 = f2_make(c1, c1);
         uint32_t s_uses = 0, o_uses = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
             const int u = unit_index(p, i);
             const int4 U = p.units[u];
             if (t >= U.w) continue;
-            const int nkv = (p.row_ptr[U.y + 1] - p.row_ptr[U.y]) * tpb;
+            const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
             const int qt = U.z + t;
             const int rows_valid = min(kQTile, p.block - qt * kQTile);
             const bool valid = r < rows_valid;
@@ -406,23 +464,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 continue;
             }
             float mrow;  // bound: m_i (natural units); online: running max in log2 units
-            float m2;
-            if constexpr (ONLINE) {
+            if constexpr (ONLINE)
                 mrow = -INFINITY;
-                m2 = 0.0f;
-            } else {
+            else
                 mrow = valid ? p.rowbound[grow] : 0.0f;
-                m2 = mrow * 1.4426950408889634f;
-            }
-            float l0 = 0.0f, l1 = 0.0f;
+            const float m2b = mrow * 1.4426950408889634f;
+            uint64_t nm2x2 = f2_make(-m2b, -m2b);
+            uint64_t la = f2_make(0.0f, 0.0f), lb = la;
             for (int j = 0; j < nkv; ++j) {
+                const int w = p.tiles[t0 + j].y;
                 ok = mbar_wait(bar.s_full + t, s_uses & 1, bar.abort, status, kStatusTimeout, tmo);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 ++s_uses;
                 tc_fence_after();
                 if constexpr (ONLINE) {
-                    const float mx = tile_row_max<N>(tS) * c1;
+                    const float mx = tile_row_max(tS, w) * c1;
                     if (j == 0) {
                         mrow = mx;
                     } else {
@@ -432,14 +489,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if (__any_sync(0xFFFFFFFFu, need)) {
                             const float alpha = need ? ex2_approx(mrow - mx) : 1.0f;
                             if (need) mrow = mx;
-                            l0 *= alpha;
-                            l1 *= alpha;
+                            const uint64_t a2 = f2_make(alpha, alpha);
+                            la = f2_mul(la, a2);
+                            lb = f2_mul(lb, a2);
                             rescale_o_row<D>(tO, alpha);
                         }
                     }
-                    m2 = mrow;
+                    nm2x2 = f2_make(-mrow, -mrow);
                 }
-                softmax_tile_bound<N>(tS, c1, m2, l0, l1);
+                softmax_tile(tS, w, c1x2, nm2x2, la, lb);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar.p_full + t);
@@ -450,28 +508,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) break;
             ++o_uses;
             tc_fence_after();
-            const float l = l0 + l1;
+            float l0, l1, l2, l3;
+            f2_split(la, l0, l1);
+            f2_split(lb, l2, l3);
+            const float l = (l0 + l1) + (l2 + l3);
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            const uint64_t inv2 = f2_make(inv, inv);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[16], b[16];
-                tmem_ld16(tO + c * 32, a);
-                tmem_ld16(tO + c * 32 + 16, b);
+                uint32_t a[32];
+                tmem_ld32(tO + c * 32, a);
                 tmem_wait_ld();
-                reg_fence16(a);
-                reg_fence16(b);
-                uint32_t w[16];
+                reg_fence32(a);
+                uint32_t wv[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * inv, __uint_as_float(a[2 * e + 1]) * inv);
-                    w[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]) * inv, __uint_as_float(b[2 * e + 1]) * inv);
+                for (int e = 0; e < 16; ++e) {
+                    float x0, x1;
+                    f2_split(f2_mul(f2_from_bits(a[2 * e], a[2 * e + 1]), inv2), x0, x1);
+                    wv[e] = pack_bf16x2(x0, x1);
                 }
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                    dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+                    dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
                 }
             }
             if (valid && p.lse) {
@@ -496,31 +557,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tc_fence_before();
+        cta_barrier();
     }
 }
 
-template <int D, int N, bool ONLINE>
+template <int D, bool ONLINE>
 cudaError_t launch_fwd_instance(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const AttnParams &p, int n_ctas, cudaStream_t s) {
-    bsattn_fwd_kernel<D, N, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D, N>::SMEM, s>>>(tq, tk, tv, p);
+    bsattn_fwd_kernel<D, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D>::SMEM, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
-template <int D, int N>
-cudaError_t configure_instance() {
-    cudaError_t e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         AttnCfg<D, N>::SMEM);
+// The register split in the kernel is valid only if it launches with exactly
+// kLaunchRegs registers per thread; refuse to configure (and so to run) otherwise.
+template <int D, bool ONLINE>
+cudaError_t configure_one() {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, bsattn_fwd_kernel<D, ONLINE>);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(bsattn_fwd_kernel<D, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                AttnCfg<D, N>::SMEM);
+    if ((a.numRegs + 7) / 8 * 8 != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(bsattn_fwd_kernel<D, ONLINE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                AttnCfg<D>::SMEM);
+}
+
+template <int D>
+cudaError_t configure_instance() {
+    cudaError_t e = configure_one<D, false>();
+    return e != cudaSuccess ? e : configure_one<D, true>();
 }
 
 }  // namespace bsv

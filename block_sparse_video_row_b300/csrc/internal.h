@@ -10,8 +10,12 @@ struct bsattn_layout_s;
 namespace bsv {
 
 constexpr int kQTile = 128;           // query rows per tile (the MMA M dimension)
-constexpr int kMaxKvTile = 128;       // keys per tile, upper bound (TMEM: 2 S + 2 O accumulators)
+constexpr int kKvTile = 128;          // keys per full key tile (TMEM: 2 S + 2 O accumulators of 128 columns)
 constexpr int kAttnThreads = 384;     // 12 warps: TMA, MMA, 2 idle, 2 softmax warpgroups
+constexpr int kLaunchRegs = 168;      // registers per thread at launch (65536 / 384, rounded down to 8)
+constexpr int kRegsLow = 72;          // TMA / MMA warpgroup after setmaxnreg.dec
+constexpr int kRegsHigh = 208;        // softmax warpgroups after setmaxnreg.inc
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kAttnThreads * kLaunchRegs, "register split");
 constexpr float kGuardTau = 5.421010862427522e-20f;  // 2^-64: smallest denominator trusted
 constexpr int kStatusTimeout = 1;     // bit in the device status word
 
@@ -33,8 +37,8 @@ enum AttnMode : int32_t {
 struct AttnParams {
     const int4 *units;        // (b*H + h, qb, first q tile, tiles in unit)
     int32_t n_units;
-    const int32_t *row_ptr;   // allowed key blocks per query block (CSR)
-    const int32_t *col_idx;
+    const int32_t *tile_ptr;  // key tiles of query block qb: tiles[tile_ptr[qb] .. tile_ptr[qb+1])
+    const int2 *tiles;        // (first key within the head, width: a multiple of 16, <= kKvTile)
     const float *rowbound;    // [B*H*L]
     uint16_t *o;              // [B*H*L, D] bf16 bits
     float *lse;               // [B*H*L] or null
@@ -64,17 +68,16 @@ cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s);
 cudaError_t launch_rowbound(const BoundsParams &p, cudaStream_t s);
 int bounds_chunk_rows();
 
-// Attention kernel for head dim D and key tile N; grid = n_ctas persistent CTAs.
+// Attention kernel for head dim D; grid = n_ctas persistent CTAs.
 cudaError_t launch_attention_d64(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 const AttnParams &p, int N, bool online, int n_ctas, cudaStream_t s);
+                                 const AttnParams &p, bool online, int n_ctas, cudaStream_t s);
 cudaError_t launch_attention_d128(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                  const AttnParams &p, int N, bool online, int n_ctas, cudaStream_t s);
-// Raise the dynamic shared-memory limit of both variants for (D, N).
-cudaError_t configure_attention_d64(int N);
-cudaError_t configure_attention_d128(int N);
-// Dynamic shared memory of one CTA for (D, N).
-size_t smem_attention_d64(int N);
-size_t smem_attention_d128(int N);
+                                  const AttnParams &p, bool online, int n_ctas, cudaStream_t s);
+// Check the register count of both variants for head dim D and raise their dynamic
+// shared-memory limit (an error if the compiled register count does not match the
+// register split the kernel performs).
+cudaError_t configure_attention_d64();
+cudaError_t configure_attention_d128();
 
 // TMA tensor maps of Q (3-D, frame-local boxes) and K, V (2-D) for a layout's shape;
 // works for plan-only layouts too.  False if the driver entry point is missing or

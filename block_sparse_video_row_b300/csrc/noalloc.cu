@@ -89,24 +89,24 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     bsattn_layout_info_t info;
     bsattn_layout_info(plan, &info);
     const size_t n = static_cast<size_t>(info.n_units);
-    const size_t nnz = static_cast<size_t>(info.nnz_blocks > 0 ? info.nnz_blocks : 1);
+    const size_t ntiles = static_cast<size_t>(info.key_tiles > 0 ? info.key_tiles : 1);
 
     // Scratch layout: guard workspace (8 header ints: status, -, -, -, fallback count,
     // fallback rows, -, -; then per-unit flags; then the fallback list), the work list,
-    // the allowed-block CSR.  Sizes beyond the array are rejected here, before any
-    // device work.
+    // the key-tile table.  Sizes beyond the array are rejected here, before any device
+    // work.
     const size_t off_units = align256((8 + 2 * n) * 4);
-    const size_t off_rowptr = align256(off_units + 16 * n);
-    const size_t off_colidx = align256(off_rowptr + 4 * (static_cast<size_t>(info.nb) + 1));
-    const size_t total = off_colidx + 4 * nnz;
+    const size_t off_tileptr = align256(off_units + 16 * n);
+    const size_t off_tiles = align256(off_tileptr + 4 * (static_cast<size_t>(info.nb) + 1));
+    const size_t total = off_tiles + 8 * ntiles;
     if (total > kNoallocScratchBytes) {
         bsattn_destroy(plan);
         return BSATTN_ERR_UNSUPPORTED;
     }
     std::vector<unsigned char> host(total, 0);
-    bsattn_layout_export(plan, reinterpret_cast<int32_t *>(host.data() + off_rowptr),
-                         reinterpret_cast<int32_t *>(host.data() + off_colidx),
-                         reinterpret_cast<int32_t *>(host.data() + off_units));
+    bsattn_layout_export(plan, nullptr, nullptr, reinterpret_cast<int32_t *>(host.data() + off_units),
+                         reinterpret_cast<int32_t *>(host.data() + off_tileptr),
+                         reinterpret_cast<int32_t *>(host.data() + off_tiles));
 
     int dev = -1;
     DeviceState *ds = nullptr;
@@ -124,8 +124,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
         bsattn_destroy(plan);
         return BSATTN_ERR_CUDA;
     }
-    cudaError_t e = info.D == 128 ? bsv::configure_attention_d128(info.kv_tile)
-                                  : bsv::configure_attention_d64(info.kv_tile);
+    cudaError_t e = info.D == 128 ? bsv::configure_attention_d128() : bsv::configure_attention_d64();
     bsattn_destroy(plan);
     if (e != cudaSuccess) return BSATTN_ERR_CUDA;
 
@@ -140,8 +139,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     bsv::AttnParams p;
     p.units = reinterpret_cast<const int4 *>(base + off_units);
     p.n_units = info.n_units;
-    p.row_ptr = reinterpret_cast<const int32_t *>(base + off_rowptr);
-    p.col_idx = reinterpret_cast<const int32_t *>(base + off_colidx);
+    p.tile_ptr = reinterpret_cast<const int32_t *>(base + off_tileptr);
+    p.tiles = reinterpret_cast<const int2 *>(base + off_tiles);
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
@@ -162,8 +161,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.timeout_ns = ms * 1000000ull;
     const int grid = std::max(1, std::min(info.n_units, ds->num_sms));
     auto launch = [&](bool on) {
-        return info.D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, info.kv_tile, on, grid, s)
-                             : bsv::launch_attention_d64(tq, tk, tv, p, info.kv_tile, on, grid, s);
+        return info.D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, on, grid, s)
+                             : bsv::launch_attention_d64(tq, tk, tv, p, on, grid, s);
     };
     if (online) {
         p.mode = bsv::kModeOnlineAll;

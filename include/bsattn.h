@@ -96,10 +96,13 @@ enum {
  *   block_mask  host pointer, nb * nb bytes, nb = L / block_size.
  *   flags       0, or BSATTN_PLAN_ONLY.
  * The plan: the allowed key blocks of each query block in ascending order;
- * the key tile (the largest multiple of 16 that divides block_size, at most
- * 128, so tiles never straddle a frame edge); query tiles of 128 rows that
- * never straddle a frame edge (the last tile of a frame may be partial); and a
- * work list of pairs of query tiles of one frame, sorted by cost, largest first.
+ * the key tiles of each query block (its allowed blocks grouped into runs of
+ * consecutive frames, each run cut into tiles of 128 keys and one last tile of
+ * the remaining keys: a multiple of 16, because frames are, so every tile is
+ * an exactly sized MMA with no element mask or padding and none reaches into a
+ * masked frame); query tiles of 128 rows that never straddle a frame edge (the
+ * last tile of a frame may be partial); and a work list of pairs of query
+ * tiles of one frame, sorted by cost, largest first.
  * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA, OOM or DEVICE.
  */
 bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,
@@ -160,10 +163,10 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
  *   q, k, v, o, scale, rowbound, lse, flags: as for bsattn_forward (device pointers;
  *             rowbound from bsattn_row_bounds or any equal bound).
  *   B, H, L, D, block_size, block_mask: as for bsattn_create_layout (mask on the host).
- * Limits: the plan (work units x 24 bytes + the allowed-block table, each part
- * rounded up to 256 bytes) must fit in the array, about 40,000 work units (the
- * 720p chunk uses 4,680, the 1080p chunk 9,984); a larger problem returns
- * BSATTN_ERR_UNSUPPORTED before any device work.
+ * Limits: the plan (work units x 24 bytes + the key-tile table, 8 bytes per
+ * tile, each part rounded up to 256 bytes) must fit in the array, about 40,000
+ * work units (the 720p chunk uses 4,680, the 1080p chunk 9,984); a larger
+ * problem returns BSATTN_ERR_UNSUPPORTED before any device work.
  * The first call on a device (with that device current) looks up the array's
  * device address; make that first call before any stream capture.  Each call
  * copies the plan and zeroed guard counters into the array with one
@@ -202,7 +205,8 @@ typedef struct {
     int32_t B, H, D, block_size, nb;
     int64_t L;
     int32_t nnz_blocks;        /* allowed (query block, key block) pairs */
-    int32_t kv_tile;           /* keys per tile */
+    int32_t kv_tile;           /* keys per full key tile (128) */
+    int32_t key_tiles;         /* key tiles over all query blocks */
     int32_t q_tiles_per_block; /* ceil(block_size / 128) */
     int32_t n_units;           /* work units (pairs of query tiles of one frame) */
     int64_t mma_rows;          /* query rows the MMAs process, partial tiles included */
@@ -215,9 +219,12 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
  * Copy the plan to host arrays (any may be NULL):
  *   row_ptr  int32 [nb + 1], col_idx int32 [nnz_blocks]: allowed key blocks per query block, ascending;
  *   units    int32 [n_units * 4]: (b * H + h, query block, first query tile, tiles in the unit (1 or 2)),
- *            in execution order.
+ *            in execution order;
+ *   tile_ptr int32 [nb + 1], tiles int32 [key_tiles * 2]: the key tiles of query block qb are
+ *            (tiles[2t], tiles[2t+1]) = (first key within the head, width) for t in [tile_ptr[qb], tile_ptr[qb+1]).
  */
-bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units);
+bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units,
+                                   int32_t *tile_ptr, int32_t *tiles);
 
 #ifdef __cplusplus
 }

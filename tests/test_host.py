@@ -34,8 +34,21 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
-def _expected_kv_tile(bs):
-    return max(n for n in range(16, 129, 16) if bs % n == 0)
+def check_tiles(mask, bs, tile_ptr, tiles):
+    """Key tiles of each query frame: exactly its allowed keys, in order; widths a multiple
+    of 16 and at most 128; a tile never spans a masked frame; within a run of consecutive
+    allowed frames every tile but the last is 128 keys."""
+    nb = mask.shape[0]
+    for qb in range(nb):
+        t = tiles[tile_ptr[qb]:tile_ptr[qb + 1]]
+        keys = np.concatenate([np.arange(s, s + w) for s, w in t]) if len(t) else np.zeros(0, int)
+        allowed = np.concatenate([np.arange(kb * bs, (kb + 1) * bs) for kb in range(nb) if mask[qb, kb]]
+                                 ) if mask[qb].any() else np.zeros(0, int)
+        assert np.array_equal(keys, allowed)
+        assert np.all(t[:, 1] % 16 == 0) and np.all((t[:, 1] >= 16) & (t[:, 1] <= 128))
+        for (s, w), nxt in zip(t, list(t[1:]) + [None]):
+            if nxt is not None and nxt[0] == s + w:   # same run continues
+                assert w == 128
 
 
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
@@ -44,12 +57,12 @@ def test_plan_matches_oracle(lib, name):
     mask = w.block_mask()
     lay = bsattn.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, bsattn.BSATTN_PLAN_ONLY)
     info = lay.info
-    row_ptr, col_idx, units = bsattn.bsattn_layout_export(lay)
+    row_ptr, col_idx, units, tile_ptr, tiles = bsattn.bsattn_layout_export(lay, with_tiles=True)
     orp, oci = oracle.allowed_csr(mask)
     assert np.array_equal(row_ptr, orp) and np.array_equal(col_idx, oci)
     assert info.nnz_blocks == len(oci) and info.nb == w.nb
-    assert info.kv_tile == _expected_kv_tile(w.block)
-    assert w.block % info.kv_tile == 0 and info.kv_tile % 16 == 0
+    assert info.kv_tile == 128 and info.key_tiles == len(tiles)
+    check_tiles(mask, w.block, tile_ptr, tiles)
     nqt = -(-w.block // 128)
     assert info.q_tiles_per_block == nqt
     assert abs(info.useful_flop - synth.useful_flop(w)) == 0
@@ -60,8 +73,8 @@ def test_plan_matches_oracle(lib, name):
         seen[bh, qb, qt0:qt0 + nt] += 1
     assert np.all(seen == 1)
     # largest cost first
-    nkv = np.diff(orp)[units[:, 1]] * (w.block // info.kv_tile)
-    cost = nkv * units[:, 3]
+    keys = np.diff(orp)[units[:, 1]] * w.block + 32 * np.diff(tile_ptr)[units[:, 1]]
+    cost = keys * units[:, 3]
     assert np.all(np.diff(cost) <= 0)
     lay.destroy()
 
@@ -74,8 +87,8 @@ def test_plan_edge_shapes(lib):
         if nb > 1:
             mask[1, :] = 0
         lay = bsattn.bsattn_create_layout(2, 3, L, 64, bs, mask, bsattn.BSATTN_PLAN_ONLY)
-        assert lay.info.kv_tile == _expected_kv_tile(bs)
-        _, _, units = bsattn.bsattn_layout_export(lay)
+        _, _, units, tile_ptr, tiles = bsattn.bsattn_layout_export(lay, with_tiles=True)
+        check_tiles(mask, bs, tile_ptr, tiles)
         assert len(units) == lay.info.n_units == 6 * nb * ((-(-bs // 128) + 1) // 2)
 
 
