@@ -17,22 +17,28 @@
 // One CTA per SM processes work units: a unit is one or two 128-row query tiles
 // of the same frame (they share every K/V tile), looping over the frame's key
 // tiles.
-//   warp 0     TMA producer: Q tiles, then a ring of STAGES K and V tiles.
-//   warp 1     MMA issuer (one thread): S_t = Q_t K^T (A, B from smem) and
-//              O_t += P_t V (A = P_t from TMEM, B = V from smem), t = 0, 1.
-//   warps 4-7  softmax of query tile 0; warps 8-11 of tile 1 (one row per thread).
+//   warp 0      TMA producer: Q tiles, then a ring of STAGES K and V tiles.
+//   warps 1, 2  MMA issuers (one thread each), one per query tile t = warp - 1:
+//               S_t = Q_t K^T (A, B from smem) and O_t += P_t V (A = P_t from
+//               TMEM, B = V from smem).  Two issuers keep one tile's MMAs from
+//               queueing behind the other tile's issue loop.
+//   warps 4-11  softmax and epilogue.  Warp w reads TMEM lanes 32*(w%4).. (its
+//               rows) and column half h = (w-4)/4 of the key tile, so all eight
+//               warps work on one query tile at a time: tile 0's softmax runs
+//               while the tensor cores run tile 1's MMAs, and vice versa.
 // TMEM (512 columns): S_0/P_0 at column 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
-// P_t (bf16, two per 32-bit column) overwrites the first w/2 columns of S_t.
+// P (bf16, two per 32-bit column) of key half h overwrites the first 32 of that
+// half's 64 S columns: keys 64h + 2c, 64h + 2c + 1 sit in column 64h + c.
 //
-// Per key tile the MMA thread issues, in order, PV_0(j), S_0(j+1), PV_1(j),
-// S_1(j+1): while softmax 0 works on S_0 the tensor cores run tile 1's MMAs and
-// vice versa.  tcgen05 MMAs from one thread complete in issue order, so the
-// commit that signals S_t(j+1) also guarantees PV_t(j) has finished: O_t is
-// stable whenever its softmax holds S_t (the online variant rescales it then).
+// Issuer t issues, per key tile j, PV_t(j) then S_t(j+1).  tcgen05 MMAs from one
+// thread complete in issue order, so the commit that signals S_t(j+1) also
+// guarantees that PV_t(j) has finished: O_t is stable whenever its softmax holds
+// S_t (the online variant rescales it then).  Each K/V stage is released by both
+// issuers (a tile absent from a unit still takes part, without MMAs).
 //
-// Every mbarrier wait is bounded (a wall-clock limit); on expiry the CTA raises
-// a shared abort flag and a device status bit, lets in-flight copies and MMAs
-// land, frees its TMEM and returns.
+// Every wait is bounded (a wall-clock limit, mbarriers only: no named barrier
+// inside the loops); on expiry the CTA raises a shared abort flag and a device
+// status bit, lets in-flight copies and MMAs land, frees its TMEM and returns.
 #pragma once
 
 #include "internal.h"
@@ -50,7 +56,9 @@ struct AttnCfg {
     static constexpr int HALF_KV = N * 128;
     static constexpr int KV_TILE = DH * HALF_KV;
     static constexpr int SMEM_CAP = 232448;           // 227 KB per CTA
-    static constexpr int RESERVED = 2048;             // alignment slack + barrier block
+    static constexpr int BAR_BYTES = 512;             // mbarriers, TMEM slot, abort flag
+    static constexpr int XCHG_BYTES = 2 * 2 * kQTile * 4;  // row exchange: [parity][half][row] fp32
+    static constexpr int RESERVED = 1024 + BAR_BYTES + XCHG_BYTES;  // + alignment slack
     static constexpr int STAGES_FIT = (SMEM_CAP - RESERVED - 2 * Q_TILE) / (2 * KV_TILE);
     static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
     static_assert(STAGES >= 2, "shared memory");
@@ -58,9 +66,11 @@ struct AttnCfg {
     static constexpr int OFF_K = 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
-    static constexpr int SMEM_USED = OFF_BAR + RESERVED;
+    static constexpr int OFF_XCHG = OFF_BAR + BAR_BYTES;
+    static constexpr int SMEM_USED = OFF_XCHG + XCHG_BYTES + 1024;
     // Above half of the SM's shared memory, so one CTA (and one TMEM owner) per SM.
     static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+    static_assert(SMEM <= SMEM_CAP, "shared memory");
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
     // QK^T descriptor without its N field (set per tile from the tile's width).
     static constexpr uint32_t IDESC_QK0 = idesc_bf16_f32(kQTile, 16, false, false) & ~(0x3Fu << 17);
@@ -69,13 +79,18 @@ struct AttnCfg {
 
 // Barrier block layout (uint64 slots).
 struct Bars {
-    uint64_t *q_full, *q_empty, *s_full, *p_full, *o_full, *k_full, *k_empty, *v_full, *v_empty, *drain;
+    uint64_t *q_full, *q_empty, *s_full, *p_full, *o_full, *drain, *xbar;
+    uint64_t *k_full, *k_empty, *v_full, *v_empty;
     uint32_t *tmem_slot;
     volatile int *abort;
+    float *xchg;  // [2 parity][2 half][kQTile rows]
 };
 
+constexpr int kSoftmaxWarps = 8;
+constexpr int kIssuers = 2;
+
 template <int STAGES>
-__device__ __forceinline__ Bars carve_bars(uint8_t *base) {
+__device__ __forceinline__ Bars carve_bars(uint8_t *base, uint8_t *xchg) {
     uint64_t *b = reinterpret_cast<uint64_t *>(base);
     Bars r;
     r.q_full = b + 0;
@@ -84,12 +99,14 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base) {
     r.p_full = b + 6;
     r.o_full = b + 8;
     r.drain = b + 10;
-    r.k_full = b + 12;
+    r.xbar = b + 12;  // one per TMEM lane quarter
+    r.k_full = b + 16;
     r.k_empty = r.k_full + STAGES;
     r.v_full = r.k_empty + STAGES;
     r.v_empty = r.v_full + STAGES;
     r.tmem_slot = reinterpret_cast<uint32_t *>(r.v_empty + STAGES);
     r.abort = reinterpret_cast<volatile int *>(r.tmem_slot + 1);
+    r.xchg = reinterpret_cast<float *>(xchg);
     return r;
 }
 
@@ -113,7 +130,7 @@ __device__ __forceinline__ void cta_barrier() {
 }
 
 // ----------------------------------------------------------------------------------------------
-// softmax of one S tile (one row per thread), P written back to TMEM as bf16
+// softmax of one column half of an S tile (one row per thread), P written back to TMEM as bf16
 
 // Two logits -> two probabilities: P = 2^(S*c1 - m2) with c1 = scale*log2(e) and
 // m2 = the row shift in log2 units; returns them as packed bf16 and adds the
@@ -127,53 +144,54 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
     return pk;
 }
 
-// One S tile of w columns (a multiple of 16, <= 128): TMEM loads of 32 columns are
-// double-buffered so the load of group g+1 overlaps the arithmetic of group g.
-// P of group g (16 packed columns) overwrites S columns [16g, 16g+16), all of
-// which were loaded by then; the load in flight reads columns >= 32(g+1).
-__device__ __forceinline__ void softmax_tile(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, uint64_t &la,
+// S columns [tS, tS + w), w a multiple of 16 and at most 64: two TMEM loads of 32
+// columns, the second in flight while the first is converted.  P of the first 32
+// keys goes to columns [tS, tS + 16) and of the next 32 to [tS + 16, tS + 32): both
+// were loaded by then, and the load in flight reads columns >= tS + 32.
+__device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, uint64_t &la,
                                              uint64_t &lb) {
+    if (w <= 0) return;
     uint32_t buf[2][32];
     if (w >= 32)
         tmem_ld32(tS, buf[0]);
     else
         tmem_ld16_into32(tS, buf[0]);
 #pragma unroll
-    for (int g = 0; g < kKvTile / 32; ++g) {
+    for (int g = 0; g < 2; ++g) {
         if (32 * g < w) {
             const bool full = w - 32 * g >= 32;
             tmem_wait_ld();
-            reg_fence32(buf[g & 1]);
-            if (32 * (g + 1) < w) {
-                if (w - 32 * (g + 1) >= 32)
-                    tmem_ld32(tS + 32 * (g + 1), buf[(g + 1) & 1]);
+            reg_fence32(buf[g]);
+            if (g == 0 && w > 32) {
+                if (w >= 64)
+                    tmem_ld32(tS + 32, buf[1]);
                 else
-                    tmem_ld16_into32(tS + 32 * (g + 1), buf[(g + 1) & 1]);
+                    tmem_ld16_into32(tS + 32, buf[1]);
             }
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                pk[e] = softmax_pair(buf[g & 1][2 * e], buf[g & 1][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
+                pk[e] = softmax_pair(buf[g][2 * e], buf[g][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
             if (full) {
 #pragma unroll
                 for (int e = 8; e < 16; ++e)
-                    pk[e] = softmax_pair(buf[g & 1][2 * e], buf[g & 1][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
+                    pk[e] = softmax_pair(buf[g][2 * e], buf[g][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
                 tmem_st16(tS + 16 * g, pk);
             } else {
-                uint32_t h[8];
+                uint32_t hh[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) h[e] = pk[e];
-                tmem_st8(tS + 16 * g, h);
+                for (int e = 0; e < 8; ++e) hh[e] = pk[e];
+                tmem_st8(tS + 16 * g, hh);
             }
         }
     }
 }
 
-// Row max of one S tile (raw logits), for the online-max variant.
-__device__ __forceinline__ float tile_row_max(uint32_t tS, int w) {
+// Row max of S columns [tS, tS + w) (raw logits), for the online-max variant; -inf if w == 0.
+__device__ __forceinline__ float half_row_max(uint32_t tS, int w) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int g = 0; g < kKvTile / 32; ++g) {
+    for (int g = 0; g < 2; ++g) {
         if (32 * g < w) {
             uint32_t a[32];
             const bool full = w - 32 * g >= 32;
@@ -194,12 +212,12 @@ __device__ __forceinline__ float tile_row_max(uint32_t tS, int w) {
     return mx;
 }
 
-// Multiply one row of the O accumulator (D fp32 columns) by alpha (warp-collective).
-template <int D>
-__device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
+// Multiply NC fp32 columns of one row of the O accumulator by alpha (warp-collective).
+template <int NC>
+__device__ __forceinline__ void rescale_o_cols(uint32_t tO, float alpha) {
     const uint64_t a2 = f2_make(alpha, alpha);
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < NC / 32; ++c) {
         uint32_t a[32];
         tmem_ld32(tO + c * 32, a);
         tmem_wait_ld();
@@ -221,6 +239,25 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
     tmem_wait_st();
 }
 
+// The two warps that own the same rows (same TMEM lane quarter q, column halves 0 and
+// 1) swap one fp32 value per row through shared memory.  The slot alternates with the
+// parity of the exchange count, which both warps advance together; a warp can reach
+// exchange n + 2 only after its partner has arrived at n + 1, i.e. after the partner
+// has read slot n.  Returns false if the bounded wait gave up.
+__device__ __forceinline__ bool pair_exchange(const Bars &bar, int q, int h, int r, uint32_t &uses, float mine,
+                                              float &other, int *status, uint64_t tmo) {
+    const uint32_t par = uses & 1;
+    float *slot = bar.xchg + par * (2 * kQTile);
+    slot[h * kQTile + r] = mine;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar.xbar + q);
+    bool ok = mbar_wait(bar.xbar + q, par, bar.abort, status, kStatusTimeout, tmo);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    ++uses;
+    other = slot[(1 - h) * kQTile + r];
+    return ok;
+}
+
 // ----------------------------------------------------------------------------------------------
 
 template <int D, bool ONLINE>
@@ -233,7 +270,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Bars bar = carve_bars<C::STAGES>(smem + C::OFF_BAR);
+    Bars bar = carve_bars<C::STAGES>(smem + C::OFF_BAR, smem + C::OFF_XCHG);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -242,16 +279,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(bar.q_full + t, 1);
             mbar_init(bar.q_empty + t, 1);
             mbar_init(bar.s_full + t, 1);
-            mbar_init(bar.p_full + t, 128);
+            mbar_init(bar.p_full + t, kSoftmaxWarps);
             mbar_init(bar.o_full + t, 1);
+            mbar_init(bar.drain + t, 1);
         }
-        mbar_init(bar.drain, 1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mbar_init(bar.xbar + q, 2);
 #pragma unroll
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(bar.k_full + s, 1);
-            mbar_init(bar.k_empty + s, 1);
+            mbar_init(bar.k_empty + s, kIssuers);
             mbar_init(bar.v_full + s, 1);
-            mbar_init(bar.v_empty + s, 1);
+            mbar_init(bar.v_empty + s, kIssuers);
         }
         *bar.abort = 0;
         fence_mbar_init();
@@ -330,52 +369,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (uint32_t x = (gv > C::STAGES ? gv - C::STAGES : 0); x < gv; ++x)
                     mbar_drain(bar.v_full + x % C::STAGES, (x / C::STAGES) & 1, tmo);
             }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
-            const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-            const uint32_t k_base = smem_u32(smem + C::OFF_K);
-            const uint32_t v_base = smem_u32(smem + C::OFF_V);
-            // S_t = Q_t K^T over the first w keys of the stage (N = w in the instruction).
-            auto issue_qk = [&](int t, int s, int w) {
-                const uint32_t qa = q_base + t * C::Q_TILE;
-                const uint32_t ka = k_base + s * C::KV_TILE;
-                const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
+        } else if ((warp == 1 || warp == 2) && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer of query tile t
+            const int t = warp - 1;
+            const uint32_t dS = tmem + (t ? C::COL_S1 : C::COL_S0);
+            const uint32_t dO = tmem + (t ? C::COL_O1 : C::COL_O0);
+            // Descriptors of the first stage; a byte offset X adds X >> 4 to the start
+            // address field (shared addresses stay below 2^18, so the field never carries).
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + C::OFF_Q + t * C::Q_TILE), 16, 1024);
+            const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+            const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + C::OFF_V), C::HALF_KV, 1024);
+            // S_t = Q_t K^T over the first w keys of stage s (N = w in the instruction).
+            auto issue_qk = [&](int s, int w) {
                 const uint32_t idesc = C::IDESC_QK0 | (static_cast<uint32_t>(w >> 3) << 17);
+                const uint64_t kd = k_desc + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * C::HALF_Q + off, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * C::HALF_KV + off, 16, 1024);
-                    mma_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    const uint32_t qo = ((kk >> 2) * C::HALF_Q + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = ((kk >> 2) * C::HALF_KV + (kk & 3) * 32) >> 4;
+                    mma_ss(dS, q_desc + qo, kd + ko, idesc, kk > 0 ? 1u : 0u);
                 }
             };
-            // O_t += P_t V over the first w keys (K = w, in steps of 16).
-            auto issue_pv = [&](int t, int s, int w, bool acc) {
-                const uint32_t va = v_base + s * C::KV_TILE;
-                const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
-                const uint32_t a = tmem + (t ? C::COL_S1 : C::COL_S0);
+            // O_t += P_t V over the first w keys (K = w, in steps of 16); the P of keys
+            // 16kk .. 16kk+15 sits in S columns 64*(kk/4) + 8*(kk%4) .. +8.
+            auto issue_pv = [&](int s, int w, bool acc) {
+                const uint64_t vd = v_desc + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    if (16 * kk < w) {
-                        const uint64_t bd = smem_desc_sw128(va + kk * 16 * 128, C::HALF_KV, 1024);
-                        mma_ts(d, a + kk * 8, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-                    }
+                    if (16 * kk < w)
+                        mma_ts(dO, dS + 64 * (kk >> 2) + 8 * (kk & 3), vd + ((kk * 16 * 128) >> 4), C::IDESC_PV,
+                               (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            uint32_t q_uses0 = 0, q_uses1 = 0, p_uses0 = 0, p_uses1 = 0;
+            uint32_t q_uses = 0, p_uses = 0;
             uint32_t g = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 const int4 U = p.units[unit_index(p, i)];
                 const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
                 if (nkv == 0) continue;
-                const int nt = U.w;
-                ok = mbar_wait(bar.q_full + 0, q_uses0 & 1, bar.abort, status, kStatusTimeout, tmo);
-                ++q_uses0;
-                if (ok && nt > 1) {
-                    ok = mbar_wait(bar.q_full + 1, q_uses1 & 1, bar.abort, status, kStatusTimeout, tmo);
-                    ++q_uses1;
+                if (t >= U.w) {
+                    // This query tile is absent from the unit: release each stage without MMAs,
+                    // after its copy has landed (so the arrival counts toward the right phase).
+                    for (int j = 0; j < nkv && ok; ++j) {
+                        const uint32_t gj = g + j;
+                        const int sj = static_cast<int>(gj % C::STAGES);
+                        const uint32_t ph = (gj / C::STAGES) & 1;
+                        ok = mbar_wait(bar.k_full + sj, ph, bar.abort, status, kStatusTimeout, tmo);
+                        if (!ok) break;
+                        mbar_arrive(bar.k_empty + sj);
+                        ok = mbar_wait(bar.v_full + sj, ph, bar.abort, status, kStatusTimeout, tmo);
+                        if (!ok) break;
+                        mbar_arrive(bar.v_empty + sj);
+                    }
+                    g += nkv;
+                    continue;
                 }
+                ok = mbar_wait(bar.q_full + t, q_uses & 1, bar.abort, status, kStatusTimeout, tmo);
+                ++q_uses;
                 if (!ok) break;
                 int w_next = p.tiles[t0].y;
                 {
@@ -383,11 +434,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = mbar_wait(bar.k_full + s0, (g / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
                     if (!ok) break;
                     tc_fence_after();
-                    for (int t = 0; t < nt; ++t) {
-                        issue_qk(t, s0, w_next);
-                        mma_commit(bar.s_full + t);
-                        if (nkv == 1) mma_commit(bar.q_empty + t);
-                    }
+                    issue_qk(s0, w_next);
+                    mma_commit(bar.s_full + t);
+                    if (nkv == 1) mma_commit(bar.q_empty + t);
                     mma_commit(bar.k_empty + s0);
                 }
                 for (int j = 0; j < nkv && ok; ++j) {
@@ -400,30 +449,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (ok && more)
                         ok = mbar_wait(bar.k_full + sn, (gn / C::STAGES) & 1, bar.abort, status, kStatusTimeout,
                                        tmo);
-                    for (int t = 0; t < nt && ok; ++t) {
-                        uint32_t &pu = t ? p_uses1 : p_uses0;
-                        ok = mbar_wait(bar.p_full + t, pu & 1, bar.abort, status, kStatusTimeout, tmo);
-                        if (!ok) break;
-                        ++pu;
-                        tc_fence_after();
-                        issue_pv(t, sj, wj, j > 0);
-                        if (more) {
-                            issue_qk(t, sn, w_next);
-                            mma_commit(bar.s_full + t);
-                            if (j + 2 == nkv) mma_commit(bar.q_empty + t);
-                        } else {
-                            mma_commit(bar.o_full + t);
-                        }
-                    }
+                    if (ok) ok = mbar_wait(bar.p_full + t, p_uses & 1, bar.abort, status, kStatusTimeout, tmo);
                     if (!ok) break;
+                    ++p_uses;
+                    tc_fence_after();
+                    issue_pv(sj, wj, j > 0);
+                    if (more) {
+                        issue_qk(sn, w_next);
+                        mma_commit(bar.s_full + t);
+                        if (j + 2 == nkv) mma_commit(bar.q_empty + t);
+                    } else {
+                        mma_commit(bar.o_full + t);
+                    }
                     mma_commit(bar.v_empty + sj);
                     if (more) mma_commit(bar.k_empty + sn);
                 }
                 g += nkv;
             }
             // Every MMA issued must complete before TMEM is freed.
-            mma_commit(bar.drain);
-            mbar_drain(bar.drain, 0, tmo);
+            mma_commit(bar.drain + t);
+            mbar_drain(bar.drain + t, 0, tmo);
         }
         tc_fence_before();
         cta_barrier();
@@ -434,124 +479,166 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ---------------------------------------------------------------- softmax + epilogue
-        const int t = (warp - 4) >> 2;
-        const int wq = warp & 3;
-        const int r = wq * 32 + lane;
-        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
-        const uint32_t tO = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+        constexpr int DC = D / 2;        // O columns of one half
+        const int q = warp & 3;          // TMEM lane quarter: rows 32q .. 32q+31
+        const int h = (warp - 4) >> 2;   // key / O column half
+        const int r = q * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t tS0 = tmem + lane_base + C::COL_S0 + 64 * h;
+        const uint32_t tS1 = tmem + lane_base + C::COL_S1 + 64 * h;
+        const uint32_t tO0 = tmem + lane_base + C::COL_O0 + DC * h;
+        const uint32_t tO1 = tmem + lane_base + C::COL_O1 + DC * h;
         const float c1 = p.scale_log2;
         const uint64_t c1x2 = f2_make(c1, c1);
-        uint32_t s_uses = 0, o_uses = 0;
+        uint32_t s_uses0 = 0, s_uses1 = 0, o_uses0 = 0, o_uses1 = 0, x_uses = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
             const int u = unit_index(p, i);
             const int4 U = p.units[u];
-            if (t >= U.w) continue;
+            const int nt = U.w;
             const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
-            const int qt = U.z + t;
-            const int rows_valid = min(kQTile, p.block - qt * kQTile);
-            const bool valid = r < rows_valid;
-            const int64_t grow = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
-                                 static_cast<int64_t>(qt) * kQTile + r;
-            uint16_t *orow = p.o + grow * D;
+            const int64_t row0 = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
+                                 static_cast<int64_t>(U.z) * kQTile + r;  // this thread's row of tile 0
+            const bool valid0 = r < min(kQTile, p.block - U.z * kQTile);
+            const bool valid1 = nt > 1 && r < min(kQTile, p.block - (U.z + 1) * kQTile);
             if (nkv == 0) {  // the frame reads no key block: O = 0, LSE = -inf
-                if (valid) {
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
-                    if (p.lse) p.lse[grow] = -INFINITY;
+                for (int t = 0; t < 2; ++t) {
+                    if (t < nt && (t ? valid1 : valid0)) {
+                        const int64_t grow = row0 + t * kQTile;
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D + DC * h);
+#pragma unroll
+                        for (int c = 0; c < DC / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+                        if (p.lse && h == 0) p.lse[grow] = -INFINITY;
+                    }
                 }
                 continue;
             }
-            float mrow;  // bound: m_i (natural units); online: running max in log2 units
-            if constexpr (ONLINE)
-                mrow = -INFINITY;
-            else
-                mrow = valid ? p.rowbound[grow] : 0.0f;
-            const float m2b = mrow * 1.4426950408889634f;
-            uint64_t nm2x2 = f2_make(-m2b, -m2b);
-            uint64_t la = f2_make(0.0f, 0.0f), lb = la;
-            for (int j = 0; j < nkv; ++j) {
+            // bound: m_i (natural units); online: running max in log2 units
+            float mrow0, mrow1;
+            if constexpr (ONLINE) {
+                mrow0 = mrow1 = -INFINITY;
+            } else {
+                mrow0 = valid0 ? p.rowbound[row0] : 0.0f;
+                mrow1 = valid1 ? p.rowbound[row0 + kQTile] : 0.0f;
+            }
+            uint64_t nm0 = f2_make(-mrow0 * 1.4426950408889634f, -mrow0 * 1.4426950408889634f);
+            uint64_t nm1 = f2_make(-mrow1 * 1.4426950408889634f, -mrow1 * 1.4426950408889634f);
+            uint64_t la0 = f2_make(0.0f, 0.0f), lb0 = la0, la1 = la0, lb1 = la0;
+            for (int j = 0; j < nkv && ok; ++j) {
                 const int w = p.tiles[t0 + j].y;
-                ok = mbar_wait(bar.s_full + t, s_uses & 1, bar.abort, status, kStatusTimeout, tmo);
+                const int wh = max(0, min(64, w - 64 * h));
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (t >= nt) break;
+                    uint32_t &su = t ? s_uses1 : s_uses0;
+                    ok = mbar_wait(bar.s_full + t, su & 1, bar.abort, status, kStatusTimeout, tmo);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) break;
+                    ++su;
+                    tc_fence_after();
+                    const uint32_t tS = t ? tS1 : tS0;
+                    uint64_t &la = t ? la1 : la0;
+                    uint64_t &lb = t ? lb1 : lb0;
+                    uint64_t &nm = t ? nm1 : nm0;
+                    if constexpr (ONLINE) {
+                        float &mrow = t ? mrow1 : mrow0;
+                        float other;
+                        const float mine = half_row_max(tS, wh) * c1;
+                        ok = pair_exchange(bar, q, h, r, x_uses, mine, other, status, tmo);
+                        if (!ok) break;
+                        const float mx = fmaxf(mine, other);
+                        if (j == 0) {
+                            mrow = mx;
+                        } else {
+                            // Rescale only when the max grew by more than 2^8: a stale max
+                            // keeps P <= 2^8, exact in fp32 and bf16.
+                            const bool need = mx > mrow + 8.0f;
+                            if (__any_sync(0xFFFFFFFFu, need)) {
+                                const float alpha = need ? ex2_approx(mrow - mx) : 1.0f;
+                                if (need) mrow = mx;
+                                const uint64_t a2 = f2_make(alpha, alpha);
+                                la = f2_mul(la, a2);
+                                lb = f2_mul(lb, a2);
+                                rescale_o_cols<DC>(t ? tO1 : tO0, alpha);
+                            }
+                        }
+                        nm = f2_make(-mrow, -mrow);
+                    }
+                    softmax_half(tS, wh, c1x2, nm, la, lb);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar.p_full + t);
+                }
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (t >= nt) break;
+                uint32_t &ou = t ? o_uses1 : o_uses0;
+                ok = mbar_wait(bar.o_full + t, ou & 1, bar.abort, status, kStatusTimeout, tmo);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
-                ++s_uses;
+                ++ou;
                 tc_fence_after();
-                if constexpr (ONLINE) {
-                    const float mx = tile_row_max(tS, w) * c1;
-                    if (j == 0) {
-                        mrow = mx;
-                    } else {
-                        // Rescale only when the max grew by more than 2^8: a stale max
-                        // keeps P <= 2^8, exact in fp32 and bf16.
-                        const bool need = mx > mrow + 8.0f;
-                        if (__any_sync(0xFFFFFFFFu, need)) {
-                            const float alpha = need ? ex2_approx(mrow - mx) : 1.0f;
-                            if (need) mrow = mx;
-                            const uint64_t a2 = f2_make(alpha, alpha);
-                            la = f2_mul(la, a2);
-                            lb = f2_mul(lb, a2);
-                            rescale_o_row<D>(tO, alpha);
-                        }
+                float l0, l1, l2, l3;
+                f2_split(t ? la1 : la0, l0, l1);
+                f2_split(t ? lb1 : lb0, l2, l3);
+                const float mine = (l0 + l1) + (l2 + l3);
+                float other;
+                ok = pair_exchange(bar, q, h, r, x_uses, mine, other, status, tmo);
+                if (!ok) break;
+                const float l = h == 0 ? mine + other : other + mine;  // half 0 + half 1, in that order
+                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                const uint64_t inv2 = f2_make(inv, inv);
+                const bool valid = t ? valid1 : valid0;
+                const int64_t grow = row0 + t * kQTile;
+                uint16_t *orow = p.o + grow * D + DC * h;
+                const uint32_t tO = t ? tO1 : tO0;
+#pragma unroll
+                for (int c = 0; c < DC / 32; ++c) {
+                    uint32_t a[32];
+                    tmem_ld32(tO + c * 32, a);
+                    tmem_wait_ld();
+                    reg_fence32(a);
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1;
+                        f2_split(f2_mul(f2_from_bits(a[2 * e], a[2 * e + 1]), inv2), x0, x1);
+                        wv[e] = pack_bf16x2(x0, x1);
                     }
-                    nm2x2 = f2_make(-mrow, -mrow);
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                        dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+                        dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+                    }
                 }
-                softmax_tile(tS, w, c1x2, nm2x2, la, lb);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar.p_full + t);
-            }
-            if (!ok) break;
-            ok = mbar_wait(bar.o_full + t, o_uses & 1, bar.abort, status, kStatusTimeout, tmo);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) break;
-            ++o_uses;
-            tc_fence_after();
-            float l0, l1, l2, l3;
-            f2_split(la, l0, l1);
-            f2_split(lb, l2, l3);
-            const float l = (l0 + l1) + (l2 + l3);
-            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            const uint64_t inv2 = f2_make(inv, inv);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32];
-                tmem_ld32(tO + c * 32, a);
-                tmem_wait_ld();
-                reg_fence32(a);
-                uint32_t wv[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float x0, x1;
-                    f2_split(f2_mul(f2_from_bits(a[2 * e], a[2 * e + 1]), inv2), x0, x1);
-                    wv[e] = pack_bf16x2(x0, x1);
-                }
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-                    dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
-                    dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
-                }
-            }
-            if (valid && p.lse) {
-                if constexpr (ONLINE)
-                    p.lse[grow] = (mrow + log2f(l)) * 0.6931471805599453f;
-                else
-                    p.lse[grow] = mrow + logf(l);
-            }
-            if constexpr (!ONLINE) {
-                if (p.mode == kModeBound) {
-                    // Underflow guard: a denominator below 2^-64 (or not finite) means the bound was
-                    // too loose for exp to resolve this row; rerun its unit with the online max.
-                    const bool bad = valid && !(l >= kGuardTau && l <= 3.402823466e38f);
-                    const unsigned ballot = __ballot_sync(0xFFFFFFFFu, bad);
-                    if (ballot && lane == 0) {
-                        atomicAdd(p.ws.fb_rows, __popc(ballot));
-                        if (atomicExch(p.ws.unit_flag + u, 1) == 0) {
-                            const int pos = atomicAdd(p.ws.fb_count, 1);
-                            p.ws.fb_list[pos] = u;
+                if (h == 0) {
+                    const float mrow = t ? mrow1 : mrow0;
+                    if (valid && p.lse) {
+                        if constexpr (ONLINE)
+                            p.lse[grow] = (mrow + log2f(l)) * 0.6931471805599453f;
+                        else
+                            p.lse[grow] = mrow + logf(l);
+                    }
+                    if constexpr (!ONLINE) {
+                        if (p.mode == kModeBound) {
+                            // Underflow guard: a denominator below 2^-64 (or not finite) means the
+                            // bound was too loose for exp to resolve this row; rerun its unit with
+                            // the online max.
+                            const bool bad = valid && !(l >= kGuardTau && l <= 3.402823466e38f);
+                            const unsigned ballot = __ballot_sync(0xFFFFFFFFu, bad);
+                            if (ballot && lane == 0) {
+                                atomicAdd(p.ws.fb_rows, __popc(ballot));
+                                if (atomicExch(p.ws.unit_flag + u, 1) == 0) {
+                                    const int pos = atomicAdd(p.ws.fb_count, 1);
+                                    p.ws.fb_list[pos] = u;
+                                }
+                            }
                         }
                     }
                 }
