@@ -134,13 +134,13 @@ __device__ __forceinline__ void cta_barrier() {
 
 // Two logits -> two probabilities: P = 2^(S*c1 - m2) with c1 = scale*log2(e) and
 // m2 = the row shift in log2 units; returns them as packed bf16 and adds the
-// rounded values (the ones the P.V product uses) to the pair accumulator l2.
+// rounded values (the ones the P.V product uses) to the accumulators l0, l1.
 __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint64_t c1x2, uint64_t nm2x2,
-                                                 uint64_t &l2) {
+                                                 float &l0, float &l1) {
     float x0, x1;
     f2_split(f2_fma(f2_from_bits(s0, s1), c1x2, nm2x2), x0, x1);
     const uint32_t pk = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-    l2 = f2_add(l2, f2_from_bits(pk << 16, pk & 0xFFFF0000u));
+    add_bf16x2_to(pk, l0, l1);
     return pk;
 }
 
@@ -148,8 +148,7 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
 // columns, the second in flight while the first is converted.  P of the first 32
 // keys goes to columns [tS, tS + 16) and of the next 32 to [tS + 16, tS + 32): both
 // were loaded by then, and the load in flight reads columns >= tS + 32.
-__device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, uint64_t &la,
-                                             uint64_t &lb) {
+__device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, float (&l)[4]) {
     if (w <= 0) return;
     uint32_t buf[2][32];
     if (w >= 32)
@@ -171,11 +170,13 @@ __device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, 
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                pk[e] = softmax_pair(buf[g][2 * e], buf[g][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
+                pk[e] = softmax_pair(buf[g][2 * e], buf[g][2 * e + 1], c1x2, nm2x2, l[2 * (e & 1)],
+                                     l[2 * (e & 1) + 1]);
             if (full) {
 #pragma unroll
                 for (int e = 8; e < 16; ++e)
-                    pk[e] = softmax_pair(buf[g][2 * e], buf[g][2 * e + 1], c1x2, nm2x2, (e & 1) ? lb : la);
+                    pk[e] = softmax_pair(buf[g][2 * e], buf[g][2 * e + 1], c1x2, nm2x2, l[2 * (e & 1)],
+                                         l[2 * (e & 1) + 1]);
                 tmem_st16(tS + 16 * g, pk);
             } else {
                 uint32_t hh[8];
@@ -524,7 +525,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             uint64_t nm0 = f2_make(-mrow0 * 1.4426950408889634f, -mrow0 * 1.4426950408889634f);
             uint64_t nm1 = f2_make(-mrow1 * 1.4426950408889634f, -mrow1 * 1.4426950408889634f);
-            uint64_t la0 = f2_make(0.0f, 0.0f), lb0 = la0, la1 = la0, lb1 = la0;
+            // row-sum accumulators: key 4i + k of a half goes to lt[k]
+            float lt0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, lt1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             for (int j = 0; j < nkv && ok; ++j) {
                 const int w = p.tiles[t0 + j].y;
                 const int wh = max(0, min(64, w - 64 * h));
@@ -538,8 +540,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ++su;
                     tc_fence_after();
                     const uint32_t tS = t ? tS1 : tS0;
-                    uint64_t &la = t ? la1 : la0;
-                    uint64_t &lb = t ? lb1 : lb0;
+                    float(&lt)[4] = t ? lt1 : lt0;
                     uint64_t &nm = t ? nm1 : nm0;
                     if constexpr (ONLINE) {
                         float &mrow = t ? mrow1 : mrow0;
@@ -557,15 +558,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             if (__any_sync(0xFFFFFFFFu, need)) {
                                 const float alpha = need ? ex2_approx(mrow - mx) : 1.0f;
                                 if (need) mrow = mx;
-                                const uint64_t a2 = f2_make(alpha, alpha);
-                                la = f2_mul(la, a2);
-                                lb = f2_mul(lb, a2);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) lt[k] *= alpha;
                                 rescale_o_cols<DC>(t ? tO1 : tO0, alpha);
                             }
                         }
                         nm = f2_make(-mrow, -mrow);
                     }
-                    softmax_half(tS, wh, c1x2, nm, la, lb);
+                    softmax_half(tS, wh, c1x2, nm, lt);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -582,10 +582,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (!ok) break;
                 ++ou;
                 tc_fence_after();
-                float l0, l1, l2, l3;
-                f2_split(t ? la1 : la0, l0, l1);
-                f2_split(t ? lb1 : lb0, l2, l3);
-                const float mine = (l0 + l1) + (l2 + l3);
+                const float(&lt)[4] = t ? lt1 : lt0;
+                const float mine = (lt[0] + lt[1]) + (lt[2] + lt[3]);
                 float other;
                 ok = pair_exchange(bar, q, h, r, x_uses, mine, other, status, tmo);
                 if (!ok) break;

@@ -281,6 +281,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
 }
+// acc + (the low / high bf16 of a packed pair), one fp32 add with a bf16 source operand
+// (sm_100 family): the bf16 value converts exactly, the sum rounds to nearest even.
+__device__ __forceinline__ void add_bf16x2_to(uint32_t pk, float &acc_lo, float &acc_hi) {
+    unsigned short lo, hi;
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(pk));
+    asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(acc_lo) : "h"(lo));
+    asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(acc_hi) : "h"(hi));
+}
 __device__ __forceinline__ float bf16lo_f32(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf16hi_f32(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
