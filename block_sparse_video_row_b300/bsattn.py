@@ -32,6 +32,8 @@ BSATTN_ERR_DEVICE = 7
 BSATTN_BOUND = 0
 BSATTN_ONLINE_MAX = 1
 BSATTN_NO_FALLBACK = 2
+BSATTN_BOUND_ONLY = 4
+BSATTN_ELIGIBLE_BOUND = 64.0
 BSATTN_PLAN_ONLY = 0x10
 
 EXPORTED = ("bsattn_create_layout", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",

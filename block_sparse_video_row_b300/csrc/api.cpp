@@ -319,7 +319,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
                              bsattn_stream_t stream) {
     bsattn_status st = check_runnable(lay);
     if (st != BSATTN_OK) return st;
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK)) != 0) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY)) != 0) return BSATTN_ERR_INVALID_ARG;
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BSATTN_ERR_INVALID_ARG;
@@ -348,6 +348,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.block = lay->bs;
     p.nb = lay->nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
     p.timeout_ns = lay->timeout_ns;
     const int grid = std::max(1, std::min(lay->n_units, lay->num_sms));
     auto launch = [&](bool on) {

@@ -515,13 +515,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 continue;
             }
-            // bound: m_i (natural units); online: running max in log2 units
+            // Per query tile, this warp's 32 rows take the bound softmax when all of them
+            // are eligible (bound at most elig_m), else the running max.  The decision is
+            // warp-uniform and equal in both column halves (same rows, same bounds).
+            // mrow: bound m_i (natural units) or the running max (log2 units).
             float mrow0, mrow1;
+            bool on0, on1;
             if constexpr (ONLINE) {
+                on0 = on1 = true;
                 mrow0 = mrow1 = -INFINITY;
             } else {
-                mrow0 = valid0 ? p.rowbound[row0] : 0.0f;
-                mrow1 = valid1 ? p.rowbound[row0 + kQTile] : 0.0f;
+                const float b0 = valid0 ? p.rowbound[row0] : 0.0f;
+                const float b1 = valid1 ? p.rowbound[row0 + kQTile] : 0.0f;
+                on0 = __any_sync(0xFFFFFFFFu, b0 > p.elig_m);
+                on1 = __any_sync(0xFFFFFFFFu, b1 > p.elig_m);
+                mrow0 = on0 ? -INFINITY : b0;
+                mrow1 = on1 ? -INFINITY : b1;
             }
             uint64_t nm0 = f2_make(-mrow0 * 1.4426950408889634f, -mrow0 * 1.4426950408889634f);
             uint64_t nm1 = f2_make(-mrow1 * 1.4426950408889634f, -mrow1 * 1.4426950408889634f);
@@ -542,7 +551,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t tS = t ? tS1 : tS0;
                     float(&lt)[4] = t ? lt1 : lt0;
                     uint64_t &nm = t ? nm1 : nm0;
-                    if constexpr (ONLINE) {
+                    if (t ? on1 : on0) {
                         float &mrow = t ? mrow1 : mrow0;
                         float other;
                         const float mine = half_row_max(tS, wh) * c1;
@@ -617,14 +626,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 if (h == 0) {
                     const float mrow = t ? mrow1 : mrow0;
+                    const bool on = t ? on1 : on0;
                     if (valid && p.lse) {
-                        if constexpr (ONLINE)
+                        if (on)
                             p.lse[grow] = (mrow + log2f(l)) * 0.6931471805599453f;
                         else
                             p.lse[grow] = mrow + logf(l);
                     }
                     if constexpr (!ONLINE) {
-                        if (p.mode == kModeBound) {
+                        if (p.mode == kModeBound && !on) {
                             // Underflow guard: a denominator below 2^-64 (or not finite) means the
                             // bound was too loose for exp to resolve this row; rerun its unit with
                             // the online max.

@@ -47,6 +47,7 @@ struct AttnParams {
     int32_t block;            // tokens per frame block
     int32_t nb;
     float scale_log2;         // scale * log2(e)
+    float elig_m;             // rows with a larger bound use the online max (kModeBound only)
     int32_t mode;
     uint64_t timeout_ns;
 };

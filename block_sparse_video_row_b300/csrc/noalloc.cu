@@ -73,7 +73,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
                                                 int32_t H, int64_t L, int32_t D, int32_t block_size,
                                                 const uint8_t *block_mask, float scale, const float *rowbound,
                                                 float *lse, int32_t flags, bsattn_stream_t stream) {
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK)) != 0) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY)) != 0) return BSATTN_ERR_INVALID_ARG;
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
     const auto mis16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) != 0; };
@@ -153,6 +153,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.block = block_size;
     p.nb = info.nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
     uint64_t ms = 4000;
     if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
         const long long val = std::atoll(env);

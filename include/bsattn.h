@@ -68,8 +68,11 @@ typedef enum {
 
 /* flags */
 enum {
-    /* bsattn_forward: bound softmax + underflow guard + online-max rerun of
-       flagged work units (the default). */
+    /* bsattn_forward (the default): per query tile and group of 32 rows, the
+       bound softmax when every row of the group is eligible (its bound m_i is at
+       most BSATTN_ELIGIBLE_BOUND), else the online max for that group in the
+       same launch; then the underflow guard on the bound rows and an online-max
+       rerun of the work units holding a flagged row. */
     BSATTN_BOUND = 0,
     /* bsattn_forward: run the online-max (running max + rescale) kernel over
        every work unit instead; the A/B baseline of the same kernel. */
@@ -77,10 +80,21 @@ enum {
     /* bsattn_forward: skip the rerun of flagged units (testing only: rows
        whose exponentials underflowed keep an undefined value). */
     BSATTN_NO_FALLBACK = 2,
+    /* bsattn_forward: the bound softmax for every row whatever its bound (no
+       eligibility switch); the guard and the rerun still apply. */
+    BSATTN_BOUND_ONLY = 4,
     /* bsattn_create_layout: build the host plan only, touch no device; such a
        layout can be inspected (info/export) but not run. */
     BSATTN_PLAN_ONLY = 0x10
 };
+
+/* Eligibility of a row for the bound softmax, in nats: rows with a larger
+   Cauchy-Schwarz bound are computed with the online max in the first launch.
+   Every unmasked logit satisfies S_ij >= -m_i, so the denominator of a bound row
+   is at least exp(-2 m_i): a row with m_i <= 22 can never trip the guard, and
+   above 64 a row passes it only if its best logit lies within 44 nats of a
+   bound of more than 64, which the data this kernel serves rarely shows. */
+#define BSATTN_ELIGIBLE_BOUND 64.0f
 
 /* Limits checked by bsattn_create_layout. */
 #define BSATTN_MAX_NB 4096            /* frames (blocks) per sequence */
@@ -134,10 +148,14 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
  *   rowbound  fp32 [B, H, L] from bsattn_row_bounds (unused with BSATTN_ONLINE_MAX; may be NULL then).
  *   lse       optional fp32 [B, H, L] out: the natural log of the softmax denominator,
  *             ln sum_j exp(scale * q_i . k_j) over allowed keys (-inf for rows that read nothing).
- *   flags     BSATTN_BOUND (0), BSATTN_ONLINE_MAX, and/or BSATTN_NO_FALLBACK.
+ *   flags     BSATTN_BOUND (0), BSATTN_ONLINE_MAX, BSATTN_NO_FALLBACK, BSATTN_BOUND_ONLY.
  * BSATTN_BOUND computes P = exp(scale * S - m_i) with no running max, rounds P
  * to bf16 for the P.V product and sums the denominator from the same rounded
- * values; a row is flagged when its denominator is below 2^-64 or not finite,
+ * values.  Each warp of the kernel owns 32 rows of a 128-row query tile; when
+ * one of them has m_i > BSATTN_ELIGIBLE_BOUND (the deep-dive's eligibility
+ * check, section 拿掉 softmax 的序列相依), that warp computes the tile with the
+ * running max instead, in the same launch (BSATTN_BOUND_ONLY turns this off).
+ * A bound row is flagged when its denominator is below 2^-64 or not finite,
  * and every work unit holding a flagged row is recomputed by the online-max
  * kernel in a second launch on the same stream (no host synchronisation).
  * Enqueued on `stream`; returns BSATTN_OK, INVALID_ARG or CUDA.

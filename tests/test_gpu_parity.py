@@ -144,22 +144,54 @@ def test_edge_shapes(ba, D, B, H, frames, bs, mask_kind):
         assert np.all(res["o"][rows] == 0) and np.all(np.isneginf(res["lse"][rows]))
 
 
-@pytest.mark.parametrize("flags", [1, 2])  # online max everywhere; bound without the rerun
+# online max everywhere; bound without the rerun; bound for every row (no eligibility switch),
+# with and without the rerun
+@pytest.mark.parametrize("flags", [1, 2, 4, 6])
 def test_variants_small(ba, flags):
     w = synth.WORKLOADS["small"]
     q, k, v = synth.make_qkv(w)
     full_case(ba, q, k, v, w.block_mask(), w.block, w.scale, flags=flags, what=f"small flags={flags}")
 
 
-def test_guard_forced_and_zero_queries(ba):
-    w = synth.WORKLOADS["tiny"]
+def _scaled_key(w, factor):
     q, k, v = synth.make_qkv(w)
     k = k.copy()
-    k[0, 0, 3] = synth.f32_to_bf16_bits((synth.bf16_bits_to_f64(k[0, 0, 3]) * 1e4).astype(np.float32))
+    k[0, 0, 3] = synth.f32_to_bf16_bits((synth.bf16_bits_to_f64(k[0, 0, 3]) * factor).astype(np.float32))
+    return q, k, v
+
+
+def _predicted_flags(q, k, v, mask, bs, scale, eligible=np.inf):
+    """(must, may) counts of guard-flagged rows: a row is a bound row when every valid row of its
+    32-row group (same head, frame, 128-row query tile and 32-row quarter) has a bound <= eligible;
+    a bound row must be flagged when ln l < ln 2^-65 and may be when ln l < ln 2^-63, l being the
+    bound-shifted denominator."""
+    B, H, L, D = q.shape
+    _, lse, _ = oracle.attention(q, k, v, mask, bs, scale)
+    _, _, m32 = oracle.metadata_f32(q, k, mask, bs, scale)
+    m = m32.reshape(-1).astype(np.float64)
+    log_l = lse - m
+    r = np.arange(B * H * L)
+    pos = r % L
+    qt_per_block = (bs + 127) // 128
+    group = ((r // L) * (L // bs) + pos // bs) * (4 * qt_per_block) + (pos % bs) // 32
+    online = np.zeros(B * H * L, dtype=bool)
+    for g in np.unique(group):
+        sel = group == g
+        online[sel] = np.any(m[sel] > eligible)
+    fin = np.isfinite(log_l)
+    must = int(np.sum(~online & fin & (log_l < np.log(2.0 ** -65))))
+    may = int(np.sum(~online & fin & (log_l < np.log(2.0 ** -63))))
+    return must, may, log_l, online
+
+
+def test_guard_forced_and_zero_queries(ba):
+    # one key 1e4 times longer: rows that read it have a bound far above their best logit
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = _scaled_key(w, 1e4)
     q = q.copy()
     q[0, 1, 100:110] = 0  # zero query rows: P = 1 for every allowed key, never flagged
     mask, bs, scale = w.block_mask(), w.block, w.scale
-    res = full_case(ba, q, k, v, mask, bs, scale, what="guard")
+    res = full_case(ba, q, k, v, mask, bs, scale, flags=4, what="guard")  # bound for every row
     # rows of head 0 in frames 0 and 1 read the huge key: the bound is far too loose there
     _, lse, _ = oracle.attention(q, k, v, mask, bs, scale)
     _, _, m32 = oracle.metadata_f32(q, k, mask, bs, scale)
@@ -169,10 +201,35 @@ def test_guard_forced_and_zero_queries(ba):
     assert must <= res["fb_rows"] <= may and must > 0
     assert res["fb_units"] >= 1
     # without the rerun those rows are not trusted, the others still match
-    res2 = run_gpu(ba, q, k, v, mask, bs, scale, flags=2, want_meta=False)
+    res2 = run_gpu(ba, q, k, v, mask, bs, scale, flags=6, want_meta=False)
     ok_rows = log_l > np.log(2.0 ** -63)
     O, _, _ = oracle.attention(q, k, v, mask, bs, scale)
     check_o(res2["o"][ok_rows], O[ok_rows], "guard, unflagged rows")
+
+
+def test_eligibility_switch_takes_loose_rows_online_in_one_launch(ba):
+    # Default mode on the same inputs: the rows whose bound is above the eligibility limit are
+    # computed with the running max in the first launch, so nothing is flagged or rerun.
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = _scaled_key(w, 1e4)
+    mask, bs, scale = w.block_mask(), w.block, w.scale
+    must, may, _, online = _predicted_flags(q, k, v, mask, bs, scale, eligible=64.0)
+    assert online.any() and must == may == 0
+    res = full_case(ba, q, k, v, mask, bs, scale, flags=0, what="eligibility switch")
+    assert res["fb_rows"] == 0 and res["fb_units"] == 0
+
+
+def test_guard_fires_on_eligible_rows(ba):
+    # A key 5x longer puts the bounds of the rows that read it between 22 and 64 nats (57 at most):
+    # they stay on the bound path (eligible), and those whose best logit lies > 44 nats below the
+    # bound are flagged and rerun; the predicted count follows the 32-row grouping of the kernel.
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = _scaled_key(w, 5.0)
+    mask, bs, scale = w.block_mask(), w.block, w.scale
+    must, may, log_l, online = _predicted_flags(q, k, v, mask, bs, scale, eligible=64.0)
+    assert must > 0 and not online.any()
+    res = full_case(ba, q, k, v, mask, bs, scale, flags=0, what="guard on eligible rows")
+    assert must <= res["fb_rows"] <= may and res["fb_units"] >= 1
 
 
 def test_deterministic(ba):
@@ -195,11 +252,14 @@ def test_workload_sampled(ba, name, heads):
     check_o(res["o"][rows], O, name)
     assert np.max(np.abs(res["lse"][rows] - lse)) <= LSE_MAX
     assert np.all(np.isfinite(res["o"]))
-    if name == "stress":
-        assert res["fb_rows"] > 0 and res["fb_units"] > 0
-    else:
-        assert res["fb_rows"] == 0
+    assert res["fb_rows"] == 0  # stress: loose rows take the running max in the first launch
     assert res["status"] == 0
+    if name == "stress":
+        # the bound path for every row: the guard flags the loose rows and the rerun fixes them
+        res2 = run_gpu(ba, q, k, v, mask, w.block, w.scale, flags=4, want_meta=False)
+        check_o(res2["o"][rows], O, name + " bound only")
+        assert np.max(np.abs(res2["lse"][rows] - lse)) <= LSE_MAX
+        assert res2["fb_rows"] > 0 and res2["fb_units"] > 0 and res2["status"] == 0
 
 
 def test_dense_1080p_sampled(ba):
