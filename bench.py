@@ -288,25 +288,27 @@ def main():
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                 "launch_ms": fwd_avg, "timed": "CUDA events around each forward call inside the timed steps"}
 
-    # ---- end to end: pinned host buffers, H2D of Q,K,V + bounds + forward + D2H of O each step
+    # ---- end to end through the host-buffer entry point: each step copies Q, K, V from pinned
+    # host memory, runs bounds + forward and copies O back, chunked over (batch, head) pairs
+    # so the copies overlap the kernels
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
+        bsattn.bsattn_forward_host(lay, hq, hk, hv, ho, w.scale, None, bsattn.BSATTN_BOUND, 0, stream)
 
+    for _ in range(2):  # the first call allocates the staging buffers
+        e2e_step()
+    torch.cuda.synchronize()
     e2e_ms = timed(e2e_step, max(3, args.steps // 4))
     e2e_val = flop_step * world / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
 
-    launches_per_step = 4  # norms, rowbound, bound attention, rerun of flagged units
+    launches_per_step = 4  # norms, rowbound, bound attention, rerun of flagged units (timed region)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
             "pct_of_tensor_peak": 100.0 * value / world / peak,
             "roofline": roofline,
             "e2e": {"value": e2e_val, "unit": UNIT, "ms_per_step": float(np.mean(e2e_ms)),
-                    "h2d_bytes_per_step": 3 * int(dq.numel()) * 2, "d2h_bytes_per_step": int(o.numel()) * 2},
+                    "h2d_bytes_per_step": 3 * int(dq.numel()) * 2, "d2h_bytes_per_step": int(o.numel()) * 2,
+                    "call": "bsattn_forward_host (pinned host Q, K, V, O)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "stages_ms": {"row_bounds": float(np.mean(bounds_live)), "forward": fwd_avg},

@@ -38,7 +38,7 @@ BSATTN_PLAN_ONLY = 0x10
 
 EXPORTED = ("bsattn_create_layout", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
             "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export",
-            "bsattn_forward_noalloc")
+            "bsattn_forward_noalloc", "bsattn_forward_host")
 
 
 class LayoutInfo(ctypes.Structure):
@@ -87,6 +87,8 @@ def load(path: Optional[str] = None):
     lib.bsattn_layout_info.argtypes = [vp, ctypes.POINTER(LayoutInfo)]
     lib.bsattn_forward_noalloc.restype = i32
     lib.bsattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, i32, vp, f32, vp, vp, i32, vp]
+    lib.bsattn_forward_host.restype = i32
+    lib.bsattn_forward_host.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, i32, vp]
     lib.bsattn_layout_export.restype = i32
     lib.bsattn_layout_export.argtypes = [vp, vp, vp, vp, vp, vp]
     _lib = lib
@@ -195,6 +197,18 @@ def bsattn_forward_noalloc(q, k, v, o, B: int, H: int, L: int, D: int, block_siz
     if raise_on_error:
         _check(st, "bsattn_forward_noalloc")
     return st
+
+
+def bsattn_forward_host(lay: Layout, q, k, v, o, scale: float, lse=None, flags: int = 0,
+                        pairs_per_chunk: int = 0, stream=None) -> None:
+    """Row bounds + forward for host tensors (pinned CPU torch tensors or numpy arrays): copies,
+    kernels and copy-out pipelined per chunk of (batch, head) pairs; synchronise `stream` before
+    reading o."""
+    for x in (q, k, v, o) + ((lse,) if lse is not None else ()):
+        if hasattr(x, "is_cuda") and x.is_cuda:
+            raise TypeError("bsattn_forward_host takes host tensors")
+    _check(load().bsattn_forward_host(lay.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), float(scale), _ptr(lse),
+                                      flags, pairs_per_chunk, _stream(stream)), "bsattn_forward_host")
 
 
 def bsattn_destroy(lay: Layout) -> None:

@@ -13,28 +13,11 @@
 #include <vector>
 
 #include "internal.h"
-
-struct bsattn_layout_s {
-    int32_t B = 0, H = 0, D = 0, bs = 0, nb = 0;
-    int64_t L = 0;
-    bool plan_only = false;
-    std::vector<int32_t> row_ptr, col_idx, units;
-    std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs
-    int32_t kv_tile = 0, qt_per_block = 0, n_units = 0;
-    int64_t mma_rows = 0;
-    double useful_flop = 0.0;
-    int device = -1, num_sms = 0;
-    int32_t *d_row_ptr = nullptr, *d_col_idx = nullptr, *d_tile_ptr = nullptr;
-    int2 *d_tiles = nullptr;
-    int4 *d_units = nullptr;
-    int32_t *d_ws = nullptr;
-    bsv::Workspace ws{};
-    uint64_t timeout_ns = 0;
-};
+#include "layout.h"
 
 namespace {
 
-constexpr int kWsHeader = 8;  // int32 slots: [0] status, [4] fb_count, [5] fb_rows
+constexpr int kWsHeader = bsv::kWsHeader;
 
 bsattn_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return BSATTN_OK;
@@ -373,6 +356,8 @@ void bsattn_destroy(bsattn_layout_t lay) {
         int cur = -1;
         cudaGetDevice(&cur);
         if (cur != lay->device) cudaSetDevice(lay->device);
+        bsv::host_pipe_destroy(lay->host);
+        lay->host = nullptr;
         free_device(lay);
         if (cur != lay->device && cur >= 0) cudaSetDevice(cur);
     }

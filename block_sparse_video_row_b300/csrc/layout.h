@@ -1,0 +1,32 @@
+// The layout object behind bsattn_layout_t (shared by the C-ABI translation units).
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "internal.h"
+
+namespace bsv {
+struct HostPipe;                   // staging and streams of bsattn_forward_host (host_pipeline.cu)
+void host_pipe_destroy(HostPipe *hp);
+constexpr int kWsHeader = 8;       // int32 workspace slots: [0] status, [4] fb_count, [5] fb_rows
+}  // namespace bsv
+
+struct bsattn_layout_s {
+    int32_t B = 0, H = 0, D = 0, bs = 0, nb = 0;
+    int64_t L = 0;
+    bool plan_only = false;
+    std::vector<int32_t> row_ptr, col_idx, units;
+    std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs
+    int32_t kv_tile = 0, qt_per_block = 0, n_units = 0;
+    int64_t mma_rows = 0;
+    double useful_flop = 0.0;
+    int device = -1, num_sms = 0;
+    int32_t *d_row_ptr = nullptr, *d_col_idx = nullptr, *d_tile_ptr = nullptr;
+    int2 *d_tiles = nullptr;
+    int4 *d_units = nullptr;
+    int32_t *d_ws = nullptr;
+    bsv::Workspace ws{};
+    uint64_t timeout_ns = 0;
+    bsv::HostPipe *host = nullptr;  // created by the first bsattn_forward_host call
+};

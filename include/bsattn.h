@@ -165,6 +165,31 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
                              bsattn_stream_t stream);
 
 /*
+ * Row bounds and forward for tensors in host memory: the whole path of
+ * bsattn_row_bounds + bsattn_forward, including the copies.
+ *   q, k, v   host bf16 [B, H, L, D] in; o host bf16 [B, H, L, D] out.  Page-locked
+ *             (pinned) memory lets the copies run asynchronously and overlap the
+ *             kernels; pageable memory works but the copies then serialise.
+ *   scale, flags  as for bsattn_forward (BSATTN_ONLINE_MAX skips the row bounds).
+ *   lse       optional host fp32 [B, H, L] out, as for bsattn_forward.
+ *   pairs_per_chunk  (batch, head) pairs per pipeline chunk; 0 picks about eight
+ *             chunks.
+ * The (batch, head) pairs are processed in chunks: copy-in, kernels and copy-out
+ * run on three streams owned by the layout, with two sets of device staging
+ * buffers, so the copies of one chunk overlap the kernels of the next.  The first
+ * call (and a call with another chunk size) allocates the staging, about
+ * 8 * pairs_per_chunk * L * D bytes plus metadata, with the chunk layouts and
+ * streams; bsattn_destroy frees them.  Results equal bsattn_forward's on the same
+ * inputs.  The work is ordered after earlier work on `stream`, and `stream` waits
+ * for the last copy-out: synchronise `stream` before reading o.  Guard counters of
+ * the whole call are reported by bsattn_query_stats.  Returns BSATTN_OK,
+ * INVALID_ARG, OOM or CUDA.
+ */
+bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q, const void *k, const void *v, void *o,
+                                  float scale, float *lse, int32_t flags, int32_t pairs_per_chunk,
+                                  bsattn_stream_t stream);
+
+/*
  * bsattn_forward_noalloc -- the forward of bsattn_forward for callers that may not
  * allocate device memory.  The pages have no counterpart: this is a deployment
  * convenience of this library.

@@ -270,3 +270,34 @@ def test_dense_1080p_sampled(ba):
     rows = sample_rows(w.B, w.H, w.L, w.block, heads=[3], per_frame_random=0)[::3]
     O, _, _ = oracle.attention(q, k, v, mask, w.block, w.scale, rows=rows)
     check_o(res["o"][rows], O, "1080p dense")
+
+
+def _pinned(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+@pytest.mark.parametrize("name,pairs,flags", [("small", 3, 0), ("small", 0, 1), ("tiny", 1, 4)])
+def test_host_path_equals_device_path(ba, name, pairs, flags):
+    # bsattn_forward_host (pinned host tensors, chunked copies and kernels on three streams)
+    # against bsattn_forward on device copies: the same kernels per row, so identical bits.
+    # small with 3 pairs per chunk runs chunks of 3, 3 and 2 heads (two chunk layouts).
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.make_qkv(w)
+    if name == "tiny":  # a loose key, so the guard flags rows (bound softmax for every row)
+        q, k, v = _scaled_key(w, 1e4)
+    mask = w.block_mask()
+    lay = ba.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask)
+    dev = run_gpu(ba, q, k, v, mask, w.block, w.scale, flags, want_meta=False, lay=lay)
+    hq, hk, hv = _pinned(q), _pinned(k), _pinned(v)
+    ho = torch.full_like(hq, float("nan")).pin_memory()
+    hl = torch.full((w.B, w.H, w.L), float("nan"), dtype=torch.float32).pin_memory()
+    for _ in range(2):  # the second call reuses the staging and streams
+        ba.bsattn_forward_host(lay, hq, hk, hv, ho, w.scale, hl, flags, pairs)
+        torch.cuda.synchronize()
+        rows, units, status = ba.bsattn_query_stats(lay)
+        assert torch.equal(ho.view(torch.int16), dev["o_raw"].cpu().view(torch.int16))
+        assert np.array_equal(hl.numpy().reshape(-1).view(np.uint32), dev["lse"].view(np.uint32))
+        assert (rows, units, status) == (dev["fb_rows"], dev["fb_units"], 0)
+    if name == "tiny":
+        assert rows > 0
+    lay.destroy()
