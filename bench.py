@@ -95,6 +95,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def rank_workload(w, rank: int):
+    """The chunk rank `rank` processes: the same shape, its own seed (independent
+    problems, no data exchanged between ranks)."""
+    from block_sparse_video_row_b300 import synth
+    if rank == 0:
+        return w
+    return synth.Workload(w.name, w.B, w.H, w.D, w.frames, w.block, w.mask, w.keys, seed=w.seed + rank)
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The slowest rank's time: the job's time (an all-reduce MAX; identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flop_per_rank_step: float, world: int, ms_step: float) -> float:
+    """Whole-job useful TFLOP/s: the work of every rank over the slowest rank's step time."""
+    return flop_per_rank_step * world / (ms_step * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(q, k, v, w, seconds: float, seed: int = 1):
     """Time the fp64 oracle on a bounded random sample of query rows; returns (TFLOP/s, rows, secs, cores)."""
     import oracle
@@ -181,11 +206,8 @@ def main():
     _build.build()
     bsattn.load()
 
-    q, k, v = synth.make_qkv(w)
     # each rank gets an independent chunk of the same shape (weak scaling)
-    if rank > 0:
-        wr = synth.Workload(w.name, w.B, w.H, w.D, w.frames, w.block, w.mask, w.keys, seed=w.seed + rank)
-        q, k, v = synth.make_qkv(wr)
+    q, k, v = synth.make_qkv(rank_workload(w, rank))
 
     def pinned(x):
         return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -253,12 +275,9 @@ def main():
     bounds_live = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)]
     fwd_live = [evs[2 * i + 1].elapsed_time(evs[2 * i + 2]) for i in range(args.steps)]
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, "cuda")
     ms_step = ms_total / args.steps
-    value = flop_step * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flop_step, world, ms_step)
 
     # ---- A/B: the same forward with the online-max kernel everywhere, and with the bound kernel
     # alone (no rerun launch), timed back to back on the same inputs
@@ -298,7 +317,7 @@ def main():
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = timed(e2e_step, max(3, args.steps // 4))
-    e2e_val = flop_step * world / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
+    e2e_val = job_throughput(flop_step, world, max_over_ranks(float(np.mean(e2e_ms)), world, "cuda"))
 
     launches_per_step = 4  # norms, rowbound, bound attention, rerun of flagged units (timed region)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
