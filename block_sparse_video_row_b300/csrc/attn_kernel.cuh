@@ -79,7 +79,7 @@ struct AttnCfg {
 
 // Barrier block layout (uint64 slots).
 struct Bars {
-    uint64_t *q_full, *q_empty, *s_full, *p_full, *o_full, *drain, *xbar;
+    uint64_t *q_full, *q_empty, *s_full, *p_full, *p_rest, *o_full, *drain, *xbar;
     uint64_t *k_full, *k_empty, *v_full, *v_empty;
     uint32_t *tmem_slot;
     volatile int *abort;
@@ -100,7 +100,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base, uint8_t *xchg) {
     r.o_full = b + 8;
     r.drain = b + 10;
     r.xbar = b + 12;  // one per TMEM lane quarter
-    r.k_full = b + 16;
+    r.p_rest = b + 16;
+    r.k_full = b + 18;
     r.k_empty = r.k_full + STAGES;
     r.v_full = r.k_empty + STAGES;
     r.v_empty = r.v_full + STAGES;
@@ -147,9 +148,15 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
 // S columns [tS, tS + w), w a multiple of 16 and at most 64: two TMEM loads of 32
 // columns, the second in flight while the first is converted.  P of the first 32
 // keys goes to columns [tS, tS + 16) and of the next 32 to [tS + 16, tS + 32): both
-// were loaded by then, and the load in flight reads columns >= tS + 32.
-__device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, float (&l)[4]) {
-    if (w <= 0) return;
+// were loaded by then, and the load in flight reads columns >= tS + 32.  mid() runs
+// once the first group's P is stored (its P.V MMAs may then start), whatever w is.
+template <typename Mid>
+__device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, float (&l)[4],
+                                             Mid &&mid) {
+    if (w <= 0) {
+        mid();
+        return;
+    }
     uint32_t buf[2][32];
     if (w >= 32)
         tmem_ld32(tS, buf[0]);
@@ -185,6 +192,7 @@ __device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, 
                 tmem_st8(tS + 16 * g, hh);
             }
         }
+        if (g == 0) mid();
     }
 }
 
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(bar.q_empty + t, 1);
             mbar_init(bar.s_full + t, 1);
             mbar_init(bar.p_full + t, kSoftmaxWarps);
+            mbar_init(bar.p_rest + t, kSoftmaxWarps);
             mbar_init(bar.o_full + t, 1);
             mbar_init(bar.drain + t, 1);
         }
@@ -392,14 +401,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             };
             // O_t += P_t V over the first w keys (K = w, in steps of 16); the P of keys
-            // 16kk .. 16kk+15 sits in S columns 64*(kk/4) + 8*(kk%4) .. +8.
-            auto issue_pv = [&](int s, int w, bool acc) {
+            // 16kk .. 16kk+15 sits in S columns 64*(kk/4) + 8*(kk%4) .. +8.  part 0 issues
+            // the k-steps of each half's first 32 keys (kk % 4 < 2), part 1 the rest.
+            auto issue_pv = [&](int s, int w, bool acc, int part) {
                 const uint64_t vd = v_desc + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    if (16 * kk < w)
+                    if (((kk >> 1) & 1) == part && 16 * kk < w)
                         mma_ts(dO, dS + 64 * (kk >> 2) + 8 * (kk & 3), vd + ((kk * 16 * 128) >> 4), C::IDESC_PV,
-                               (acc || kk > 0) ? 1u : 0u);
+                               (acc || part > 0 || kk > 0) ? 1u : 0u);
                 }
             };
             uint32_t q_uses = 0, p_uses = 0;
@@ -452,9 +462,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                        tmo);
                     if (ok) ok = mbar_wait(bar.p_full + t, p_uses & 1, bar.abort, status, kStatusTimeout, tmo);
                     if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(sj, wj, j > 0, 0);
+                    ok = mbar_wait(bar.p_rest + t, p_uses & 1, bar.abort, status, kStatusTimeout, tmo);
+                    if (!ok) break;
                     ++p_uses;
                     tc_fence_after();
-                    issue_pv(sj, wj, j > 0);
+                    issue_pv(sj, wj, j > 0, 1);
                     if (more) {
                         issue_qk(sn, w_next);
                         mma_commit(bar.s_full + t);
@@ -574,11 +588,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         nm = f2_make(-mrow, -mrow);
                     }
-                    softmax_half(tS, wh, c1x2, nm, lt);
+                    // p_full[t]: the P of every warp's first 32 keys is stored (P.V k-steps 0, 1,
+                    // 4, 5 may start); p_rest[t]: all of it is.
+                    softmax_half(tS, wh, c1x2, nm, lt, [&]() {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar.p_full + t);
+                    });
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar.p_full + t);
+                    if (lane == 0) mbar_arrive(bar.p_rest + t);
                 }
             }
             if (!ok) break;
