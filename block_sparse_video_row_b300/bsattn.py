@@ -33,6 +33,7 @@ BSATTN_BOUND = 0
 BSATTN_ONLINE_MAX = 1
 BSATTN_NO_FALLBACK = 2
 BSATTN_BOUND_ONLY = 4
+BSATTN_DEBUG_STALL = 0x100
 BSATTN_ELIGIBLE_BOUND = 64.0
 BSATTN_PLAN_ONLY = 0x10
 

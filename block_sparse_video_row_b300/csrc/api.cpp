@@ -302,7 +302,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
                              bsattn_stream_t stream) {
     bsattn_status st = check_runnable(lay);
     if (st != BSATTN_OK) return st;
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY)) != 0) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_DEBUG_STALL)) != 0)
+        return BSATTN_ERR_INVALID_ARG;
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BSATTN_ERR_INVALID_ARG;
@@ -332,6 +333,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.nb = lay->nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
+    p.debug_stall = (flags & BSATTN_DEBUG_STALL) ? 1 : 0;
     p.timeout_ns = lay->timeout_ns;
     const int grid = std::max(1, std::min(lay->n_units, lay->num_sms));
     auto launch = [&](bool on) {
@@ -347,6 +349,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     if (e != cudaSuccess) return from_cuda(e);
     if (flags & BSATTN_NO_FALLBACK) return BSATTN_OK;
     p.mode = bsv::kModeFallback;
+    p.debug_stall = 0;
     return from_cuda(launch(true));
 }
 

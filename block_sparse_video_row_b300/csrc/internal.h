@@ -49,6 +49,7 @@ struct AttnParams {
     float scale_log2;         // scale * log2(e)
     float elig_m;             // rows with a larger bound use the online max (kModeBound only)
     int32_t mode;
+    int32_t debug_stall;      // testing: skip the first unit's query-tile loads (waits run out)
     uint64_t timeout_ns;
 };
 

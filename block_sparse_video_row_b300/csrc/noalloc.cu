@@ -154,6 +154,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.nb = info.nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
+    p.debug_stall = 0;
     uint64_t ms = 4000;
     if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
         const long long val = std::atoll(env);

@@ -83,6 +83,12 @@ enum {
     /* bsattn_forward: the bound softmax for every row whatever its bound (no
        eligibility switch); the guard and the rerun still apply. */
     BSATTN_BOUND_ONLY = 4,
+    /* bsattn_forward, testing only: the first work unit of every CTA never gets
+       its query tiles, so the kernel's bounded waits run out (after the layout's
+       wait limit, BSATTN_TIMEOUT_MS at create, default 4000 ms); the kernel
+       returns, bsattn_query_stats reports BSATTN_ERR_TIMEOUT and o is undefined.
+       The GPU context stays usable. */
+    BSATTN_DEBUG_STALL = 0x100,
     /* bsattn_create_layout: build the host plan only, touch no device; such a
        layout can be inspected (info/export) but not run. */
     BSATTN_PLAN_ONLY = 0x10

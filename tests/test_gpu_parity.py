@@ -301,3 +301,20 @@ def test_host_path_equals_device_path(ba, name, pairs, flags):
     if name == "tiny":
         assert rows > 0
     lay.destroy()
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable(ba, monkeypatch):
+    # BSATTN_DEBUG_STALL withholds the first unit's query tiles in every CTA: the MMA
+    # issuers' waits run out after the layout's 200 ms limit, the CTA aborts (copies in
+    # flight drained, TMEM freed) and the kernel returns; the status word says so.
+    w = synth.WORKLOADS["small"]
+    q, k, v = synth.make_qkv(w)
+    mask = w.block_mask()
+    monkeypatch.setenv("BSATTN_TIMEOUT_MS", "200")
+    lay = ba.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask)  # reads the limit
+    monkeypatch.delenv("BSATTN_TIMEOUT_MS")
+    res = run_gpu(ba, q, k, v, mask, w.block, w.scale, flags=ba.BSATTN_DEBUG_STALL, want_meta=False, lay=lay)
+    assert res["status"] == ba.BSATTN_ERR_TIMEOUT
+    lay.destroy()
+    # the same process and context still compute correct results
+    full_case(ba, q, k, v, mask, w.block, w.scale, what="after a timeout")
