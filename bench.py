@@ -98,10 +98,10 @@ class ClockSampler:
 def rank_workload(w, rank: int):
     """The chunk rank `rank` processes: the same shape, its own seed (independent
     problems, no data exchanged between ranks)."""
-    from block_sparse_video_row_b300 import synth
+    import dataclasses
     if rank == 0:
         return w
-    return synth.Workload(w.name, w.B, w.H, w.D, w.frames, w.block, w.mask, w.keys, seed=w.seed + rank)
+    return dataclasses.replace(w, seed=w.seed + rank)
 
 
 def max_over_ranks(x: float, world: int, device="cpu") -> float:
@@ -164,13 +164,16 @@ def main():
     from block_sparse_video_row_b300 import synth
     w = synth.WORKLOADS[args.workload]
     if args.heads:
-        w = synth.Workload(f"{w.name}-h{args.heads}", w.B, args.heads, w.D, w.frames, w.block, w.mask, w.keys, w.seed)
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}-h{args.heads}", H=args.heads)
     flop_step = synth.useful_flop(w)
-    config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D, "frames": w.frames,
+    config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "L_kv": w.L_kv, "D": w.D, "frames": w.frames,
+              "query_frames": w.nq,
               "block": w.block, "mask": "frame window" + (" + first frame" if w.block_mask()[-1, 0] else ""),
               "nnz_blocks": int(w.block_mask().sum()), "keys": w.keys, "seed": w.seed,
               "useful_flop_per_step": flop_step,
-              "l2": "inputs larger than L2 (Q+K+V+O %.2f GB > 126 MB), no flush" % (4 * w.B * w.H * w.L * w.D * 2 / 1e9)}
+              "l2": "inputs larger than L2 (Q+K+V+O %.2f GB > 126 MB), no flush"
+                    % (2 * w.B * w.H * (w.L + w.L_kv) * w.D * 2 / 1e9)}
 
     if args.impl == "reference":
         if rank != 0:
@@ -215,13 +218,14 @@ def main():
     hq, hk, hv = pinned(q), pinned(k), pinned(v)
     dq, dk, dv = hq.cuda(), hk.cuda(), hv.cuda()
     B, H, L, D = q.shape
-    nb = L // w.block
+    L_kv = k.shape[2]
+    nb_kv = L_kv // w.block
     o = torch.empty_like(dq)
     ho = torch.empty_like(hq).pin_memory()
     qn = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
-    km = torch.empty((B, H, nb), dtype=torch.float32, device="cuda")
+    km = torch.empty((B, H, nb_kv), dtype=torch.float32, device="cuda")
     rb = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
-    lay = bsattn.bsattn_create_layout(B, H, L, D, w.block, w.block_mask())
+    lay = bsattn.bsattn_create_layout(B, H, L, D, w.block, w.block_mask(), L_kv=L_kv)
     stream = torch.cuda.current_stream()
 
     def step(mid=None):
@@ -326,7 +330,8 @@ def main():
             "pct_of_tensor_peak": 100.0 * value / world / peak,
             "roofline": roofline,
             "e2e": {"value": e2e_val, "unit": UNIT, "ms_per_step": float(np.mean(e2e_ms)),
-                    "h2d_bytes_per_step": 3 * int(dq.numel()) * 2, "d2h_bytes_per_step": int(o.numel()) * 2,
+                    "h2d_bytes_per_step": (int(dq.numel()) + int(dk.numel()) + int(dv.numel())) * 2,
+                    "d2h_bytes_per_step": int(o.numel()) * 2,
                     "call": "bsattn_forward_host (pinned host Q, K, V, O)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,

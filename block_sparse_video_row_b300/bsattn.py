@@ -37,7 +37,7 @@ BSATTN_DEBUG_STALL = 0x100
 BSATTN_ELIGIBLE_BOUND = 64.0
 BSATTN_PLAN_ONLY = 0x10
 
-EXPORTED = ("bsattn_create_layout", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
+EXPORTED = ("bsattn_create_layout", "bsattn_create_layout_rect", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
             "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export",
             "bsattn_forward_noalloc", "bsattn_forward_host")
 
@@ -47,7 +47,8 @@ class LayoutInfo(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("nb", ctypes.c_int32), ("L", ctypes.c_int64),
                 ("nnz_blocks", ctypes.c_int32), ("kv_tile", ctypes.c_int32), ("key_tiles", ctypes.c_int32),
                 ("q_tiles_per_block", ctypes.c_int32), ("n_units", ctypes.c_int32),
-                ("mma_rows", ctypes.c_int64), ("useful_flop", ctypes.c_double)]
+                ("mma_rows", ctypes.c_int64), ("useful_flop", ctypes.c_double), ("L_kv", ctypes.c_int64),
+                ("nb_kv", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -74,6 +75,8 @@ def load(path: Optional[str] = None):
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     lib.bsattn_create_layout.restype = i32
     lib.bsattn_create_layout.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i32, i32, vp, i32]
+    lib.bsattn_create_layout_rect.restype = i32
+    lib.bsattn_create_layout_rect.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i64, i32, i32, vp, i32]
     lib.bsattn_row_bounds.restype = i32
     lib.bsattn_row_bounds.argtypes = [vp, vp, vp, f32, vp, vp, vp, vp]
     lib.bsattn_forward.restype = i32
@@ -158,15 +161,28 @@ class Layout:
 
 
 def bsattn_create_layout(B: int, H: int, L: int, D: int, block_size: int, block_mask, flags: int = 0,
-                         raise_on_error: bool = True):
-    """Returns a Layout (or, with raise_on_error=False, the pair (status, Layout or None))."""
+                         raise_on_error: bool = True, L_kv: Optional[int] = None):
+    """Returns a Layout (or, with raise_on_error=False, the pair (status, Layout or None)).
+    L_kv (key tokens, default L) other than L builds a streamed-chunk layout through
+    bsattn_create_layout_rect; block_mask is then [L / block_size, L_kv / block_size]."""
     m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
     h = ctypes.c_void_p()
-    st = load().bsattn_create_layout(ctypes.byref(h), B, H, L, D, block_size, m.ctypes.data, flags)
+    if L_kv is None or L_kv == L:
+        st = load().bsattn_create_layout(ctypes.byref(h), B, H, L, D, block_size, m.ctypes.data, flags)
+        what = "bsattn_create_layout"
+    else:
+        st = load().bsattn_create_layout_rect(ctypes.byref(h), B, H, L, L_kv, D, block_size, m.ctypes.data, flags)
+        what = "bsattn_create_layout_rect"
     if not raise_on_error:
         return st, (Layout(h.value, m) if st == BSATTN_OK else None)
-    _check(st, "bsattn_create_layout")
+    _check(st, what)
     return Layout(h.value, m)
+
+
+def bsattn_create_layout_rect(B: int, H: int, L: int, L_kv: int, D: int, block_size: int, block_mask,
+                              flags: int = 0, raise_on_error: bool = True):
+    """A streamed-chunk layout: L query tokens reading L_kv key tokens."""
+    return bsattn_create_layout(B, H, L, D, block_size, block_mask, flags, raise_on_error, L_kv=L_kv)
 
 
 def bsattn_row_bounds(lay: Layout, q, k, scale: float, qnorm, kmax, rowbound, stream=None,
@@ -260,10 +276,11 @@ def attention(q, k, v, block_mask, block_size: int, scale: Optional[float] = Non
     """O = block-sparse attention of bf16 [B,H,L,D] CUDA tensors (allocates O, metadata and LSE with torch)."""
     import torch
     B, H, L, D = q.shape
+    L_kv = k.shape[2]
     if scale is None:
         scale = float(np.float32(1.0 / np.sqrt(D)))
-    lay = layout or bsattn_create_layout(B, H, L, D, block_size, block_mask)
-    nb = L // block_size
+    lay = layout or bsattn_create_layout(B, H, L, D, block_size, block_mask, L_kv=L_kv)
+    nb = L_kv // block_size
     dev = q.device
     o = torch.empty_like(q)
     qnorm = torch.empty((B, H, L), dtype=torch.float32, device=dev)

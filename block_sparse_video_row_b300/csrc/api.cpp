@@ -28,11 +28,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     const int32_t nb = lay.nb;
+    const int32_t nbkv = lay.nbkv;
     lay.row_ptr.assign(static_cast<size_t>(nb) + 1, 0);
     lay.col_idx.clear();
     for (int32_t qb = 0; qb < nb; ++qb) {
-        for (int32_t kb = 0; kb < nb; ++kb)
-            if (mask[static_cast<int64_t>(qb) * nb + kb]) lay.col_idx.push_back(kb);
+        for (int32_t kb = 0; kb < nbkv; ++kb)
+            if (mask[static_cast<int64_t>(qb) * nbkv + kb]) lay.col_idx.push_back(kb);
         lay.row_ptr[qb + 1] = static_cast<int32_t>(lay.col_idx.size());
     }
     // Key tiles: the allowed key blocks of a query block, grouped into runs of
@@ -129,11 +130,11 @@ bool encode_q_map(CUtensorMap *m, const bsattn_layout_s &lay, const void *ptr) {
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// K and V viewed as [B*H*L rows][D].  A box of kv_tile rows starts at a key tile; when the
+// K and V viewed as [B*H*L_kv rows][D].  A box of kv_tile rows starts at a key tile; when the
 // tile is the narrower last one of a run, the rows past it are loaded but never used.
 bool encode_kv_map(CUtensorMap *m, const bsattn_layout_s &lay, const void *ptr) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lay.D),
-                                static_cast<cuuint64_t>(lay.B) * lay.H * static_cast<cuuint64_t>(lay.L)};
+                                static_cast<cuuint64_t>(lay.B) * lay.H * static_cast<cuuint64_t>(lay.Lkv)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lay.D) * 2};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(lay.kv_tile)};
     const cuuint32_t es[2] = {1, 1};
@@ -231,15 +232,20 @@ extern "C" {
 
 bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,
                                    int32_t block_size, const uint8_t *block_mask, int32_t flags) {
+    return bsattn_create_layout_rect(out, B, H, L, L, D, block_size, block_mask, flags);
+}
+
+bsattn_status bsattn_create_layout_rect(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int64_t L_kv,
+                                        int32_t D, int32_t block_size, const uint8_t *block_mask, int32_t flags) {
     if (!out) return BSATTN_ERR_INVALID_ARG;
     *out = nullptr;
-    if (!block_mask || B < 1 || H < 1 || L < 1 || block_size < 1) return BSATTN_ERR_INVALID_ARG;
+    if (!block_mask || B < 1 || H < 1 || L < 1 || L_kv < 1 || block_size < 1) return BSATTN_ERR_INVALID_ARG;
     if ((flags & ~BSATTN_PLAN_ONLY) != 0) return BSATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
-    if (block_size % 16 != 0 || L % block_size != 0) return BSATTN_ERR_UNALIGNED_BLOCK;
-    const int64_t nb = L / block_size;
-    if (nb > BSATTN_MAX_NB) return BSATTN_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(B) * H * L > BSATTN_MAX_ROWS) return BSATTN_ERR_UNSUPPORTED;
+    if (block_size % 16 != 0 || L % block_size != 0 || L_kv % block_size != 0) return BSATTN_ERR_UNALIGNED_BLOCK;
+    const int64_t nb = L / block_size, nbkv = L_kv / block_size;
+    if (nb > BSATTN_MAX_NB || nbkv > BSATTN_MAX_NB) return BSATTN_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(B) * H * std::max(L, L_kv) > BSATTN_MAX_ROWS) return BSATTN_ERR_UNSUPPORTED;
 
     bsattn_layout_s *lay = new (std::nothrow) bsattn_layout_s;
     if (!lay) return BSATTN_ERR_OOM;
@@ -247,9 +253,11 @@ bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, i
         lay->B = B;
         lay->H = H;
         lay->L = L;
+        lay->Lkv = L_kv;
         lay->D = D;
         lay->bs = block_size;
         lay->nb = static_cast<int32_t>(nb);
+        lay->nbkv = static_cast<int32_t>(nbkv);
         lay->plan_only = (flags & BSATTN_PLAN_ONLY) != 0;
         build_plan(*lay, block_mask);
     } catch (const std::bad_alloc &) {
@@ -286,12 +294,14 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
     p.row_ptr = lay->d_row_ptr;
     p.col_idx = lay->d_col_idx;
     p.L = lay->L;
+    p.Lkv = lay->Lkv;
     p.block = lay->bs;
     p.nb = lay->nb;
+    p.nbkv = lay->nbkv;
     p.BH = lay->B * lay->H;
     p.chunks_per_block = (lay->bs + bsv::bounds_chunk_rows() - 1) / bsv::bounds_chunk_rows();
     p.scale = scale;
-    cudaError_t e = cudaMemsetAsync(kmax, 0, static_cast<size_t>(p.BH) * lay->nb * 4, s);
+    cudaError_t e = cudaMemsetAsync(kmax, 0, static_cast<size_t>(p.BH) * lay->nbkv * 4, s);
     if (e == cudaSuccess) e = bsv::launch_norms(p, lay->D, s);
     if (e == cudaSuccess) e = bsv::launch_rowbound(p, s);
     return from_cuda(e);
@@ -329,6 +339,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.lse = lse;
     p.ws = lay->ws;
     p.L = lay->L;
+    p.Lkv = lay->Lkv;
     p.block = lay->bs;
     p.nb = lay->nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -411,6 +422,8 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
     info->n_units = lay->n_units;
     info->mma_rows = lay->mma_rows;
     info->useful_flop = lay->useful_flop;
+    info->L_kv = lay->Lkv;
+    info->nb_kv = lay->nbkv;
     return BSATTN_OK;
 }
 

@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                     (U.z + t) * kQTile, U.x * p.nb + U.y, bar.q_full + t, pol_q);
                 }
                 for (int j = 0; j < nkv && ok; ++j, ++g) {
-                    const int row = static_cast<int>(static_cast<int64_t>(U.x) * p.L) + p.tiles[t0 + j].x;
+                    const int row = static_cast<int>(static_cast<int64_t>(U.x) * p.Lkv) + p.tiles[t0 + j].x;
                     const int s = static_cast<int>(g % C::STAGES);
                     const uint32_t ph = (g / C::STAGES) & 1;
                     ok = mbar_wait(bar.k_empty + s, ph ^ 1, bar.abort, status, kStatusTimeout, tmo);

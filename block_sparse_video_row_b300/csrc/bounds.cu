@@ -16,7 +16,8 @@
 // then a correctly rounded square root.
 //
 // HBM-bound: Q and K are each read once with 16-byte (D=128) or 8-byte (D=64)
-// coalesced loads; a 16-lane group covers one row, a warp two rows.
+// coalesced loads; a 16-lane group covers one row, a warp two rows.  Q has L rows
+// per head and K L_kv (more than L for a streamed chunk reading context frames).
 #include "internal.h"
 
 namespace bsv {
@@ -56,44 +57,48 @@ __device__ __forceinline__ float tree16(float s, unsigned mask) {
     return s;
 }
 
+// One CTA per (row chunk of one block) of Q (the first BH * nb * chunks CTAs) or of K
+// (the rest): Q chunks write their rows' norms, K chunks fold theirs into the block's max.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) norms_kernel(const BoundsParams p) {
     constexpr int PER = D / 16;
     const int cpb = p.chunks_per_block;
-    const int chunk = static_cast<int>(blockIdx.x % cpb);
-    const int64_t seg = blockIdx.x / cpb;  // (b*H + h) * nb + kb
-    const int kb = static_cast<int>(seg % p.nb);
-    const int64_t bh = seg / p.nb;
-    const int64_t row0 = bh * p.L + static_cast<int64_t>(kb) * p.block + static_cast<int64_t>(chunk) * kChunkRows;
+    const int64_t q_ctas = static_cast<int64_t>(p.BH) * p.nb * cpb;
+    const bool is_q = static_cast<int64_t>(blockIdx.x) < q_ctas;
+    const int64_t id = is_q ? blockIdx.x : blockIdx.x - q_ctas;
+    const int nblk = is_q ? p.nb : p.nbkv;
+    const int64_t L = is_q ? p.L : p.Lkv;
+    const int chunk = static_cast<int>(id % cpb);
+    const int64_t seg = id / cpb;  // (b*H + h) * nblk + blk
+    const int blk = static_cast<int>(seg % nblk);
+    const int64_t bh = seg / nblk;
+    const int64_t row0 = bh * L + static_cast<int64_t>(blk) * p.block + static_cast<int64_t>(chunk) * kChunkRows;
     const int nrows = min(kChunkRows, p.block - chunk * kChunkRows);  // a multiple of 16
+    const uint16_t *x = is_q ? p.q : p.k;
     const int lane16 = threadIdx.x & 15;
     const int grp = threadIdx.x >> 4;
     const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
 
     float kmax = 0.0f;
-    constexpr int U = 4;  // rows per group in flight
+    constexpr int U = 8;  // rows per group in flight
     for (int r = grp; r < nrows; r += 16 * U) {
-        uint32_t wq[U][PER / 2], wk[U][PER / 2];
+        uint32_t w[U][PER / 2];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (r + 16 * u < nrows) load_chunk<PER>(x + (row0 + r + 16 * u) * D + lane16 * PER, w[u]);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (r + 16 * u < nrows) {
-                const int64_t off = (row0 + r + 16 * u) * D + lane16 * PER;
-                load_chunk<PER>(p.q + off, wq[u]);
-                load_chunk<PER>(p.k + off, wk[u]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (r + 16 * u < nrows) {
-                const float qs = tree16(chunk_sumsq<PER>(wq[u]), gmask);
-                const float ks = tree16(chunk_sumsq<PER>(wk[u]), gmask);
-                const float qn = __fsqrt_rn(qs);
-                const float kn = __fsqrt_rn(ks);
-                if (lane16 == 0) p.qnorm[row0 + r + 16 * u] = qn;
-                kmax = kn > kmax ? kn : kmax;
+                const float n = __fsqrt_rn(tree16(chunk_sumsq<PER>(w[u]), gmask));
+                if (is_q) {
+                    if (lane16 == 0) p.qnorm[row0 + r + 16 * u] = n;
+                } else {
+                    kmax = n > kmax ? n : kmax;
+                }
             }
         }
     }
+    if (is_q) return;  // uniform per CTA
     // CTA max of the key norms, then one atomic per CTA (norms are >= 0, so the
     // unsigned order of the fp32 bit patterns is the numeric order).
 #pragma unroll
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsPara
     if (threadIdx.x == 0) {
         float m = 0.0f;
         for (int e = p.row_ptr[qb]; e < p.row_ptr[qb + 1]; ++e) {
-            const float x = __uint_as_float(p.kmax_bits[bh * p.nb + p.col_idx[e]]);
+            const float x = __uint_as_float(p.kmax_bits[bh * p.nbkv + p.col_idx[e]]);
             m = x > m ? x : m;
         }
         kB = m;
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsPara
 }
 
 cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s) {
-    const int64_t grid = static_cast<int64_t>(p.BH) * p.nb * p.chunks_per_block;
+    const int64_t grid = static_cast<int64_t>(p.BH) * (p.nb + p.nbkv) * p.chunks_per_block;
     if (D == 128)
         norms_kernel<128><<<static_cast<unsigned>(grid), kNormThreads, 0, s>>>(p);
     else

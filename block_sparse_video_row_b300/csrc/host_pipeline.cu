@@ -76,18 +76,20 @@ bsattn_status host_pipe_create(const bsattn_layout_s &lay, int32_t G, HostPipe *
     const int32_t BH = lay.B * lay.H;
     hp->G = G;
     hp->G_last = BH - (BH - 1) / G * G;
-    std::vector<uint8_t> mask(static_cast<size_t>(lay.nb) * lay.nb, 0);
+    std::vector<uint8_t> mask(static_cast<size_t>(lay.nb) * lay.nbkv, 0);
     for (int32_t qb = 0; qb < lay.nb; ++qb)
         for (int32_t e = lay.row_ptr[qb]; e < lay.row_ptr[qb + 1]; ++e)
-            mask[static_cast<size_t>(qb) * lay.nb + lay.col_idx[e]] = 1;
-    bsattn_status st = bsattn_create_layout(&hp->sub_full, 1, G, lay.L, lay.D, lay.bs, mask.data(), 0);
+            mask[static_cast<size_t>(qb) * lay.nbkv + lay.col_idx[e]] = 1;
+    bsattn_status st =
+        bsattn_create_layout_rect(&hp->sub_full, 1, G, lay.L, lay.Lkv, lay.D, lay.bs, mask.data(), 0);
     if (st == BSATTN_OK && hp->G_last != G)
-        st = bsattn_create_layout(&hp->sub_last, 1, hp->G_last, lay.L, lay.D, lay.bs, mask.data(), 0);
+        st = bsattn_create_layout_rect(&hp->sub_last, 1, hp->G_last, lay.L, lay.Lkv, lay.D, lay.bs, mask.data(), 0);
     if (st != BSATTN_OK) {
         host_pipe_destroy(hp);
         return st;
     }
-    const size_t elems = static_cast<size_t>(G) * lay.L * lay.D;
+    const size_t q_elems = static_cast<size_t>(G) * lay.L * lay.D;    // Q, O
+    const size_t kv_elems = static_cast<size_t>(G) * lay.Lkv * lay.D; // K, V
     const size_t rows = static_cast<size_t>(G) * lay.L;
     cudaError_t e = cudaSuccess;
     for (cudaStream_t *s : {&hp->s_in, &hp->s_cmp, &hp->s_out})
@@ -97,11 +99,13 @@ bsattn_status host_pipe_create(const bsattn_layout_s &lay, int32_t G, HostPipe *
     for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
         for (cudaEvent_t *ev : {&hp->ev_in[b], &hp->ev_cmp[b], &hp->ev_out[b]})
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-        for (uint16_t **p : {&hp->dq[b], &hp->dk[b], &hp->dv[b], &hp->dO[b]})
-            if (e == cudaSuccess) e = cudaMalloc(p, elems * 2);
+        for (uint16_t **p : {&hp->dq[b], &hp->dO[b]})
+            if (e == cudaSuccess) e = cudaMalloc(p, q_elems * 2);
+        for (uint16_t **p : {&hp->dk[b], &hp->dv[b]})
+            if (e == cudaSuccess) e = cudaMalloc(p, kv_elems * 2);
         for (float **p : {&hp->qn[b], &hp->rb[b], &hp->lse[b]})
             if (e == cudaSuccess) e = cudaMalloc(p, rows * 4);
-        if (e == cudaSuccess) e = cudaMalloc(&hp->km[b], static_cast<size_t>(G) * lay.nb * 4);
+        if (e == cudaSuccess) e = cudaMalloc(&hp->km[b], static_cast<size_t>(G) * lay.nbkv * 4);
     }
     if (e != cudaSuccess) {
         host_pipe_destroy(hp);
@@ -138,7 +142,8 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int32_t nc = (BH + G - 1) / G;
-    const size_t pair_elems = static_cast<size_t>(lay->L) * lay->D;
+    const size_t pair_q = static_cast<size_t>(lay->L) * lay->D;     // elements of one pair's Q or O
+    const size_t pair_kv = static_cast<size_t>(lay->Lkv) * lay->D;  // elements of one pair's K or V
 
     cudaError_t e = cudaEventRecord(hp.ev_start, cs);
     for (cudaStream_t s : {hp.s_in, hp.s_cmp, hp.s_out})
@@ -149,20 +154,20 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
         const int b = c & 1;
         const int32_t g = c == nc - 1 ? hp.G_last : G;
         bsattn_layout_t sub = g == G ? hp.sub_full : hp.sub_last;
-        const size_t off = static_cast<size_t>(c) * G * pair_elems;  // elements
-        const size_t bytes = static_cast<size_t>(g) * pair_elems * 2;
+        const size_t off_q = static_cast<size_t>(c) * G * pair_q, off_kv = static_cast<size_t>(c) * G * pair_kv;
+        const size_t bytes_q = static_cast<size_t>(g) * pair_q * 2, bytes_kv = static_cast<size_t>(g) * pair_kv * 2;
         const size_t rows = static_cast<size_t>(g) * lay->L;
         // copy in (buffer b is free once chunk c-2's kernels are done with it)
         if (c >= 2) e = cudaStreamWaitEvent(hp.s_in, hp.ev_cmp[b], 0);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(hp.dq[b], static_cast<const uint16_t *>(q) + off, bytes, cudaMemcpyHostToDevice,
+            e = cudaMemcpyAsync(hp.dq[b], static_cast<const uint16_t *>(q) + off_q, bytes_q, cudaMemcpyHostToDevice,
                                 hp.s_in);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(hp.dk[b], static_cast<const uint16_t *>(k) + off, bytes, cudaMemcpyHostToDevice,
-                                hp.s_in);
+            e = cudaMemcpyAsync(hp.dk[b], static_cast<const uint16_t *>(k) + off_kv, bytes_kv,
+                                cudaMemcpyHostToDevice, hp.s_in);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(hp.dv[b], static_cast<const uint16_t *>(v) + off, bytes, cudaMemcpyHostToDevice,
-                                hp.s_in);
+            e = cudaMemcpyAsync(hp.dv[b], static_cast<const uint16_t *>(v) + off_kv, bytes_kv,
+                                cudaMemcpyHostToDevice, hp.s_in);
         if (e == cudaSuccess) e = cudaEventRecord(hp.ev_in[b], hp.s_in);
         // compute (the output buffer is free once chunk c-2's copy-out is done)
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_cmp, hp.ev_in[b], 0);
@@ -181,7 +186,8 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
         // copy out
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_out, hp.ev_cmp[b], 0);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(static_cast<uint16_t *>(o) + off, hp.dO[b], bytes, cudaMemcpyDeviceToHost, hp.s_out);
+            e = cudaMemcpyAsync(static_cast<uint16_t *>(o) + off_q, hp.dO[b], bytes_q, cudaMemcpyDeviceToHost,
+                                hp.s_out);
         if (e == cudaSuccess && lse)
             e = cudaMemcpyAsync(lse + static_cast<size_t>(c) * G * lay->L, hp.lse[b], rows * 4,
                                 cudaMemcpyDeviceToHost, hp.s_out);

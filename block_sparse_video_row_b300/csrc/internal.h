@@ -43,9 +43,10 @@ struct AttnParams {
     uint16_t *o;              // [B*H*L, D] bf16 bits
     float *lse;               // [B*H*L] or null
     Workspace ws;
-    int64_t L;
+    int64_t L;                // query tokens per sequence (Q, O rows per head)
+    int64_t Lkv;              // key tokens per sequence (K, V rows per head)
     int32_t block;            // tokens per frame block
-    int32_t nb;
+    int32_t nb;               // query blocks
     float scale_log2;         // scale * log2(e)
     float elig_m;             // rows with a larger bound use the online max (kModeBound only)
     int32_t mode;
@@ -59,8 +60,8 @@ struct BoundsParams {
     uint32_t *kmax_bits;      // fp32 bits, zeroed before the norms launch
     float *rowbound;
     const int32_t *row_ptr, *col_idx;
-    int64_t L;
-    int32_t block, nb, BH;
+    int64_t L, Lkv;           // query / key tokens per sequence
+    int32_t block, nb, nbkv, BH;
     int32_t chunks_per_block; // row chunks per frame block
     float scale;
 };

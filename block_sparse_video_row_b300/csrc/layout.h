@@ -13,8 +13,10 @@ constexpr int kWsHeader = 8;       // int32 workspace slots: [0] status, [4] fb_
 }  // namespace bsv
 
 struct bsattn_layout_s {
-    int32_t B = 0, H = 0, D = 0, bs = 0, nb = 0;
-    int64_t L = 0;
+    int32_t B = 0, H = 0, D = 0, bs = 0, nb = 0;  // nb: query blocks
+    int64_t L = 0;                                // query tokens per sequence
+    int32_t nbkv = 0;                             // key blocks
+    int64_t Lkv = 0;                              // key tokens per sequence
     bool plan_only = false;
     std::vector<int32_t> row_ptr, col_idx, units;
     std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs

@@ -150,6 +150,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.ws.unit_flag = ws + 8;
     p.ws.fb_list = ws + 8 + n;
     p.L = L;
+    p.Lkv = L;
     p.block = block_size;
     p.nb = info.nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);

@@ -129,6 +129,13 @@ def dense_mask(nb: int) -> np.ndarray:
 
 @dataclass(frozen=True)
 class Workload:
+    """A problem shape.  ``frames`` key/value frames; the queries are the last
+    ``q_frames`` of them (0: all, self-attention over the chunk).  With
+    q_frames < frames this is a streamed chunk whose queries read earlier context
+    frames as well as the chunk: the mask is the last q_frames rows of the
+    frames x frames mask, and Q is the last q_frames frames of the full-window
+    query tensor (so its rows equal the matching rows of the self-attention
+    problem over all frames)."""
     name: str
     B: int
     H: int
@@ -138,9 +145,19 @@ class Workload:
     mask: Callable[[int], np.ndarray]
     keys: str = "normal"      # "normal" or "lognormal_outliers"
     seed: int = 0
+    q_frames: int = 0
+
+    @property
+    def nq(self) -> int:
+        return self.q_frames or self.frames
 
     @property
     def L(self) -> int:
+        """Query rows per head."""
+        return self.nq * self.tokens_per_frame
+
+    @property
+    def L_kv(self) -> int:
         return self.frames * self.tokens_per_frame
 
     @property
@@ -149,6 +166,11 @@ class Workload:
 
     @property
     def nb(self) -> int:
+        """Query frames."""
+        return self.nq
+
+    @property
+    def nb_kv(self) -> int:
         return self.frames
 
     @property
@@ -156,7 +178,8 @@ class Workload:
         return float(np.float32(1.0 / np.sqrt(self.D)))
 
     def block_mask(self) -> np.ndarray:
-        return self.mask(self.frames)
+        """uint8 [nq, frames]: the last nq rows of the frames x frames mask."""
+        return np.ascontiguousarray(self.mask(self.frames)[self.frames - self.nq:, :])
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -173,6 +196,13 @@ WORKLOADS: Dict[str, Workload] = {
     # 720p shape with keys whose per-token norms are log-normal (sigma 1.5) and 1% outliers at 8x
     "stress": Workload("stress", 1, 24, 128, 13, 3600, lambda nb: window_mask(nb, 1, True),
                        keys="lognormal_outliers"),
+    # a streamed chunk: 3 query frames of 400 tokens reading 5 context frames plus the chunk
+    # (window +-2 plus frame 0 over the 8 frames)
+    "stream_small": Workload("stream_small", 1, 8, 128, 8, 400, lambda nb: window_mask(nb, 2, True),
+                             q_frames=3),
+    # a streamed 720p chunk: 4 query frames of 3600 tokens reading 9 context frames plus the chunk
+    # (window +-1 plus frame 0 over the 13 frames)
+    "stream": Workload("stream", 1, 24, 128, 13, 3600, lambda nb: window_mask(nb, 1, True), q_frames=4),
 }
 
 
@@ -200,11 +230,14 @@ def key_row_scale(seed: int, B: int, H: int, L: int, sigma: float = 1.5,
 
 
 def make_qkv(w: Workload):
-    """(q, k, v) as uint16 bf16 bits, each [B,H,L,D]."""
-    q = tensor_bf16(w.seed, TAG_Q, w.B, w.H, w.L, w.D)
-    rs = key_row_scale(w.seed, w.B, w.H, w.L) if w.keys == "lognormal_outliers" else None
-    k = tensor_bf16(w.seed, TAG_K, w.B, w.H, w.L, w.D, rs)
-    v = tensor_bf16(w.seed, TAG_V, w.B, w.H, w.L, w.D)
+    """(q [B,H,L,D], k [B,H,L_kv,D], v [B,H,L_kv,D]) as uint16 bf16 bits; q holds the last
+    L rows of the full-window query tensor."""
+    q = tensor_bf16(w.seed, TAG_Q, w.B, w.H, w.L_kv, w.D)
+    if w.L != w.L_kv:
+        q = np.ascontiguousarray(q[:, :, w.L_kv - w.L:, :])
+    rs = key_row_scale(w.seed, w.B, w.H, w.L_kv) if w.keys == "lognormal_outliers" else None
+    k = tensor_bf16(w.seed, TAG_K, w.B, w.H, w.L_kv, w.D, rs)
+    v = tensor_bf16(w.seed, TAG_V, w.B, w.H, w.L_kv, w.D)
     return q, k, v
 
 

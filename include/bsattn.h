@@ -20,11 +20,16 @@
  *    with a running-max (online softmax) kernel (the deep-dive's per-head
  *    eligibility check with fallback to online softmax, same section).
  *
- * Tensors: Q, K, V, O are bf16, contiguous [B, H, L, D], L = nb * block_size,
- * 16-byte-aligned base addresses, on the device that was current at
- * bsattn_create_layout.  Row i of head (b, h) belongs to block i / block_size.
- * The block mask is one [nb, nb] uint8 matrix (row-major, nonzero = query block
- * qb reads key block kb), shared by every batch entry and head.  L_q = L_kv.
+ * Tensors: Q and O are bf16, contiguous [B, H, L, D] with L = nb * block_size;
+ * K and V are [B, H, L_kv, D] with L_kv = nb_kv * block_size; 16-byte-aligned
+ * base addresses, on the device that was current at layout creation.  Row i of
+ * head (b, h) belongs to block i / block_size, key j to block j / block_size.
+ * The block mask is one [nb, nb_kv] uint8 matrix (row-major, nonzero = query
+ * block qb reads key block kb), shared by every batch entry and head.
+ * Self-attention over one chunk has L_kv = L (bsattn_create_layout); a streamed
+ * chunk whose queries also read earlier context frames has L_kv > L
+ * (bsattn_create_layout_rect; the pages stream their output chunk by chunk,
+ * deep-dive, opening section).
  *
  * Ownership: the caller owns every tensor it passes (Q, K, V, O, LSE and the
  * metadata buffers).  A layout owns its host plan and its device buffers (the
@@ -103,8 +108,8 @@ enum {
 #define BSATTN_ELIGIBLE_BOUND 64.0f
 
 /* Limits checked by bsattn_create_layout. */
-#define BSATTN_MAX_NB 4096            /* frames (blocks) per sequence */
-#define BSATTN_MAX_ROWS 2147483647LL  /* B * H * L */
+#define BSATTN_MAX_NB 4096            /* frames (blocks) per sequence, query or key side */
+#define BSATTN_MAX_ROWS 2147483647LL  /* B * H * L and B * H * L_kv */
 
 /*
  * Build a layout for one problem shape and block mask.
@@ -129,12 +134,23 @@ bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, i
                                    int32_t block_size, const uint8_t *block_mask, int32_t flags);
 
 /*
+ * The same for a streamed chunk: L query tokens (the chunk) reading L_kv key
+ * tokens (context frames and the chunk).  block_mask is nb * nb_kv bytes,
+ * nb = L / block_size, nb_kv = L_kv / block_size, row-major by query block.
+ * Q and O are [B, H, L, D], K and V [B, H, L_kv, D], qnorm and rowbound
+ * [B, H, L], kmax [B, H, nb_kv].  bsattn_create_layout(..., L, ...) equals
+ * bsattn_create_layout_rect(..., L, L, ...).  Returns as bsattn_create_layout.
+ */
+bsattn_status bsattn_create_layout_rect(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int64_t L_kv,
+                                        int32_t D, int32_t block_size, const uint8_t *block_mask, int32_t flags);
+
+/*
  * The Cauchy-Schwarz row bounds (the precomputed norm table of the deep-dive,
  * section 拿掉 softmax 的序列相依).  All pointers are device pointers.
- *   q, k      bf16 [B, H, L, D].
+ *   q, k      bf16 [B, H, L, D] and [B, H, L_kv, D].
  *   scale     the softmax scale (usually 1/sqrt(D)); pass the same value to bsattn_forward.
  *   qnorm     out, fp32 [B, H, L]: |q_i|.
- *   kmax      out, fp32 [B, H, nb]: the largest |k_j| of each key block.
+ *   kmax      out, fp32 [B, H, nb_kv]: the largest |k_j| of each key block.
  *   rowbound  out, fp32 [B, H, L]: m_i = (scale * |q_i|) * max over allowed kb of kmax[kb],
  *             each product rounded to fp32 (0 for a row that reads no block).
  * Norms use one fixed fp32 rounding order: the D elements split into 16
@@ -148,7 +164,7 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
 
 /*
  * The attention forward.  All pointers are device pointers.
- *   q, k, v   bf16 [B, H, L, D] in.
+ *   q         bf16 [B, H, L, D] in; k, v bf16 [B, H, L_kv, D] in.
  *   o         bf16 [B, H, L, D] out (every row is written; rows that read no block get 0).
  *   scale     softmax scale (the value given to bsattn_row_bounds).
  *   rowbound  fp32 [B, H, L] from bsattn_row_bounds (unused with BSATTN_ONLINE_MAX; may be NULL then).
@@ -260,6 +276,8 @@ typedef struct {
     int32_t n_units;           /* work units (pairs of query tiles of one frame) */
     int64_t mma_rows;          /* query rows the MMAs process, partial tiles included */
     double useful_flop;        /* 4 * nnz_blocks * block_size^2 * D * H * B */
+    int64_t L_kv;              /* key tokens per sequence (L for self-attention) */
+    int32_t nb_kv;             /* key blocks */
 } bsattn_layout_info_t;
 
 bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info);

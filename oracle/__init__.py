@@ -48,19 +48,20 @@ def _load():
         lib = ctypes.CDLL(_LIB_PATH)
         i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
         lib.orc_allowed_csr.restype = i32
-        lib.orc_allowed_csr.argtypes = [i32, _P, _P, _P]
+        lib.orc_allowed_csr.argtypes = [i32, i32, _P, _P, _P]
         lib.orc_attention.restype = None
-        lib.orc_attention.argtypes = [i32, i32, i64, i32, i32, _P, _P, _P, _P, f64, i64, _P, _P, _P, _P, _P, i32]
+        lib.orc_attention.argtypes = [i32, i32, i64, i64, i32, i32, _P, _P, _P, _P, f64, i64, _P, _P, _P, _P, _P,
+                                      i32]
         lib.orc_row_norms_f64.restype = None
         lib.orc_row_norms_f64.argtypes = [i64, i32, _P, _P]
         lib.orc_row_bounds_f64.restype = None
-        lib.orc_row_bounds_f64.argtypes = [i32, i64, i32, _P, f64, _P, _P, _P]
+        lib.orc_row_bounds_f64.argtypes = [i32, i64, i64, i32, _P, f64, _P, _P, _P]
         lib.orc_row_norms_f32.restype = None
         lib.orc_row_norms_f32.argtypes = [i64, i32, _P, _P]
         lib.orc_block_max_f32.restype = None
         lib.orc_block_max_f32.argtypes = [i32, i32, i32, _P, _P]
         lib.orc_row_bounds_f32.restype = None
-        lib.orc_row_bounds_f32.argtypes = [i32, i64, i32, _P, f32, _P, _P, _P]
+        lib.orc_row_bounds_f32.argtypes = [i32, i64, i32, i32, _P, f32, _P, _P, _P]
         _lib = lib
     return _lib
 
@@ -80,13 +81,12 @@ def n_threads() -> int:
 
 
 def allowed_csr(mask: np.ndarray):
-    """(row_ptr[nb+1], col_idx[nnz]) of the allowed key blocks, ascending."""
+    """(row_ptr[nbq+1], col_idx[nnz]) of the allowed key blocks of each query block, ascending."""
     m = np.ascontiguousarray(mask, dtype=np.uint8)
-    nb = m.shape[0]
-    assert m.shape == (nb, nb)
-    row_ptr = np.zeros(nb + 1, dtype=np.int32)
-    col_idx = np.zeros(max(nb * nb, 1), dtype=np.int32)
-    nnz = _load().orc_allowed_csr(nb, _ptr(m), _ptr(row_ptr), _ptr(col_idx))
+    nbq, nbkv = m.shape
+    row_ptr = np.zeros(nbq + 1, dtype=np.int32)
+    col_idx = np.zeros(max(nbq * nbkv, 1), dtype=np.int32)
+    nnz = _load().orc_allowed_csr(nbq, nbkv, _ptr(m), _ptr(row_ptr), _ptr(col_idx))
     return row_ptr, col_idx[:nnz].copy()
 
 
@@ -95,14 +95,17 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, blo
               nthreads: Optional[int] = None):
     """fp64 masked softmax attention.
 
-    q, k, v: uint16 bf16 bits [B,H,L,D].  rows: global row ids into B*H*L (None = all).
+    q: uint16 bf16 bits [B,H,Lq,D]; k, v: [B,H,Lkv,D]; mask [Lq/block, Lkv/block].
+    rows: global query row ids into B*H*Lq (None = all).
     Returns (O [nrows, D] fp64, LSE [nrows], l [nrows]) where l = sum_j exp(S_ij - shift_i)
     (shift = row max when ``shift`` is None)."""
     q, k, v = _u16(q), _u16(k), _u16(v)
-    B, H, L, D = q.shape
-    assert k.shape == q.shape and v.shape == q.shape and L % block == 0
+    B, H, Lq, D = q.shape
+    Lkv = k.shape[2]
+    assert k.shape == (B, H, Lkv, D) and v.shape == k.shape and Lq % block == 0 and Lkv % block == 0
     m = np.ascontiguousarray(mask, dtype=np.uint8)
-    nrows = B * H * L if rows is None else len(rows)
+    assert m.shape == (Lq // block, Lkv // block)
+    nrows = B * H * Lq if rows is None else len(rows)
     rws = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     sh = None if shift is None else np.ascontiguousarray(shift, dtype=np.float64)
     if sh is not None:
@@ -110,7 +113,7 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, blo
     out = np.empty((nrows, D), dtype=np.float64)
     lse = np.empty(nrows, dtype=np.float64)
     lsum = np.empty(nrows, dtype=np.float64)
-    _load().orc_attention(B, H, L, D, block, _ptr(m), _ptr(q), _ptr(k), _ptr(v), float(scale), nrows,
+    _load().orc_attention(B, H, Lq, Lkv, D, block, _ptr(m), _ptr(q), _ptr(k), _ptr(v), float(scale), nrows,
                           _ptr(rws), _ptr(sh), _ptr(out), _ptr(lse), _ptr(lsum),
                           nthreads or n_threads())
     return out, lse, lsum
@@ -125,12 +128,12 @@ def row_norms_f64(x: np.ndarray) -> np.ndarray:
 
 
 def row_bounds_f64(qnorm: np.ndarray, knorm: np.ndarray, mask: np.ndarray, block: int, scale: float):
-    """M_i = scale * |q_i| * max_{j allowed} |k_j| in fp64; qnorm, knorm are [B,H,L]."""
+    """M_i = scale * |q_i| * max_{j allowed} |k_j| in fp64; qnorm [B,H,Lq], knorm [B,H,Lkv]."""
     qn = np.ascontiguousarray(qnorm, dtype=np.float64)
     kn = np.ascontiguousarray(knorm, dtype=np.float64)
-    B, H, L = qn.shape
+    B, H, Lq = qn.shape
     out = np.empty_like(qn)
-    _load().orc_row_bounds_f64(B * H, L, block, _ptr(np.ascontiguousarray(mask, dtype=np.uint8)),
+    _load().orc_row_bounds_f64(B * H, Lq, kn.shape[2], block, _ptr(np.ascontiguousarray(mask, dtype=np.uint8)),
                                float(scale), _ptr(qn), _ptr(kn), _ptr(out))
     return out
 
@@ -157,15 +160,15 @@ def block_max_f32(knorm: np.ndarray, block: int) -> np.ndarray:
 def row_bounds_f32(qnorm: np.ndarray, kmax: np.ndarray, mask: np.ndarray, block: int, scale: float):
     qn = np.ascontiguousarray(qnorm, dtype=np.float32)
     km = np.ascontiguousarray(kmax, dtype=np.float32)
-    B, H, L = qn.shape
+    B, H, Lq = qn.shape
     out = np.empty_like(qn)
-    _load().orc_row_bounds_f32(B * H, L, block, _ptr(np.ascontiguousarray(mask, dtype=np.uint8)),
+    _load().orc_row_bounds_f32(B * H, Lq, km.shape[2], block, _ptr(np.ascontiguousarray(mask, dtype=np.uint8)),
                                np.float32(scale), _ptr(qn), _ptr(km), _ptr(out))
     return out
 
 
 def metadata_f32(q: np.ndarray, k: np.ndarray, mask: np.ndarray, block: int, scale: float):
-    """(qnorm [B,H,L], kmax [B,H,nb], rowbound [B,H,L]) with the canonical fp32 recipe."""
+    """(qnorm [B,H,Lq], kmax [B,H,nbkv], rowbound [B,H,Lq]) with the canonical fp32 recipe."""
     qn = row_norms_f32(q)
     kn = row_norms_f32(k)
     km = block_max_f32(kn, block)

@@ -26,10 +26,14 @@
  * masked softmax attention.  The oracle is that definition written out, with
  * the textbook max shift, in fp64 (orc_attention with shift == NULL).
  *
- * Conventions: q, k, v are bf16 bit patterns (uint16) laid out [B,H,L,D];
- * L = nb * bs; query row i of head (b,h) lies in block i / bs; key j likewise.
- * mask is uint8 [nb, nb] row-major, mask[qb*nb + kb] != 0 means query block
- * qb reads key block kb; one mask serves every batch and head.
+ * Conventions: q is bf16 bit patterns (uint16) laid out [B,H,Lq,D], k and v
+ * [B,H,Lkv,D]; Lq = nbq * bs, Lkv = nbkv * bs; query row i of head (b,h) lies in
+ * block i / bs, key j in block j / bs.  mask is uint8 [nbq, nbkv] row-major,
+ * mask[qb*nbkv + kb] != 0 means query block qb reads key block kb; one mask
+ * serves every batch and head.  Self-attention over one chunk is Lq = Lkv; a
+ * streamed chunk whose queries read earlier context frames as well as the chunk
+ * ("HeyGen Avatar IV on Trillium TPU" deep-dive, opening section: the output is
+ * streamed chunk by chunk) has Lkv > Lq.
  */
 #include <math.h>
 #include <pthread.h>
@@ -49,12 +53,12 @@ static inline double bf16_to_f64(uint16_t b) {
  * in ascending kb order, as CSR (row_ptr[nb+1], col_idx[nnz]).  Returns nnz.
  * ([deep-dive] shrink the block to 16: the mask is decided per block.)
  */
-int32_t orc_allowed_csr(int32_t nb, const uint8_t *mask, int32_t *row_ptr, int32_t *col_idx) {
+int32_t orc_allowed_csr(int32_t nbq, int32_t nbkv, const uint8_t *mask, int32_t *row_ptr, int32_t *col_idx) {
     int32_t nnz = 0;
     row_ptr[0] = 0;
-    for (int32_t qb = 0; qb < nb; ++qb) {
-        for (int32_t kb = 0; kb < nb; ++kb)
-            if (mask[(int64_t)qb * nb + kb]) col_idx[nnz++] = kb;
+    for (int32_t qb = 0; qb < nbq; ++qb) {
+        for (int32_t kb = 0; kb < nbkv; ++kb)
+            if (mask[(int64_t)qb * nbkv + kb]) col_idx[nnz++] = kb;
         row_ptr[qb + 1] = nnz;
     }
     return nnz;
@@ -70,15 +74,15 @@ int32_t orc_allowed_csr(int32_t nb, const uint8_t *mask, int32_t *row_ptr, int32
  *   LSE_i = c_i + ln l_i
  * A row with no allowed key gets O_i = 0, LSE_i = -inf, l_i = 0.
  *
- * rows: global row ids r = (b*H + h)*L + i (NULL: all B*H*L rows, in order).
+ * rows: global query row ids r = (b*H + h)*Lq + i (NULL: all B*H*Lq rows, in order).
  * shift: per listed row (NULL: max shift).  Given the Cauchy-Schwarz bound as
  * the shift this is the method's own formulation ([deep-dive] remove softmax's
  * serial dependency); both give the same O up to rounding.
  * out: nrows x D; lse, lsum: nrows (nullable).
  */
 typedef struct {
-    int32_t H, D, bs, nb;
-    int64_t L;
+    int32_t H, D, bs, nbkv;
+    int64_t Lq, Lkv;
     const uint8_t *mask;
     const uint16_t *q, *k, *v;
     double scale;
@@ -89,23 +93,23 @@ typedef struct {
 } attn_job_t;
 
 static void attn_rows(const attn_job_t *J) {
-    const int32_t D = J->D, bs = J->bs, nb = J->nb;
-    const int64_t L = J->L;
-    double *S = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
-    int64_t *key = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
+    const int32_t D = J->D, bs = J->bs, nbkv = J->nbkv;
+    const int64_t Lq = J->Lq, Lkv = J->Lkv;
+    double *S = (double *)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
+    int64_t *key = (int64_t *)malloc(sizeof(int64_t) * (size_t)(Lkv > 0 ? Lkv : 1));
     double *qv = (double *)malloc(sizeof(double) * (size_t)D);
     double *acc = (double *)malloc(sizeof(double) * (size_t)D);
     for (int64_t r = J->r0; r < J->r1; ++r) {
         const int64_t row = J->rows ? J->rows[r] : r;
-        const int64_t bh = row / L, i = row % L;
+        const int64_t bh = row / Lq, i = row % Lq;
         const int32_t qb = (int32_t)(i / bs);
         for (int32_t d = 0; d < D; ++d) qv[d] = bf16_to_f64(J->q[row * D + d]);
 
         int64_t n = 0;
-        for (int32_t kb = 0; kb < nb; ++kb) {
-            if (!J->mask[(int64_t)qb * nb + kb]) continue;
+        for (int32_t kb = 0; kb < nbkv; ++kb) {
+            if (!J->mask[(int64_t)qb * nbkv + kb]) continue;
             for (int64_t j = (int64_t)kb * bs; j < (int64_t)(kb + 1) * bs; ++j) {
-                const uint16_t *kj = J->k + (bh * L + j) * D;
+                const uint16_t *kj = J->k + (bh * Lkv + j) * D;
                 double dot = 0.0;
                 for (int32_t d = 0; d < D; ++d) dot += qv[d] * bf16_to_f64(kj[d]);
                 S[n] = J->scale * dot;
@@ -132,7 +136,7 @@ static void attn_rows(const attn_job_t *J) {
         for (int64_t t = 0; t < n; ++t) {
             const double p = exp(S[t] - c);
             l += p;
-            const uint16_t *vj = J->v + (bh * L + key[t]) * D;
+            const uint16_t *vj = J->v + (bh * Lkv + key[t]) * D;
             for (int32_t d = 0; d < D; ++d) acc[d] += p * bf16_to_f64(vj[d]);
         }
         for (int32_t d = 0; d < D; ++d) o[d] = acc[d] / l;
@@ -147,16 +151,16 @@ static void attn_rows(const attn_job_t *J) {
 
 static void *attn_thread(void *arg) { attn_rows((const attn_job_t *)arg); return NULL; }
 
-void orc_attention(int32_t B, int32_t H, int64_t L, int32_t D, int32_t bs, const uint8_t *mask,
+void orc_attention(int32_t B, int32_t H, int64_t Lq, int64_t Lkv, int32_t D, int32_t bs, const uint8_t *mask,
                    const uint16_t *q, const uint16_t *k, const uint16_t *v, double scale,
                    int64_t nrows, const int64_t *rows, const double *shift,
                    double *out, double *lse, double *lsum, int32_t nthreads) {
     attn_job_t base;
     memset(&base, 0, sizeof base);
-    base.H = H; base.D = D; base.bs = bs; base.nb = (int32_t)(L / bs); base.L = L;
+    base.H = H; base.D = D; base.bs = bs; base.nbkv = (int32_t)(Lkv / bs); base.Lq = Lq; base.Lkv = Lkv;
     base.mask = mask; base.q = q; base.k = k; base.v = v; base.scale = scale;
     base.rows = rows; base.shift = shift; base.out = out; base.lse = lse; base.lsum = lsum;
-    if (!rows) nrows = (int64_t)B * H * L;
+    if (!rows) nrows = (int64_t)B * H * Lq;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 512) nthreads = 512;
     if (nthreads > nrows) nthreads = (int32_t)(nrows > 0 ? nrows : 1);
@@ -196,23 +200,23 @@ void orc_row_norms_f64(int64_t nrows, int32_t D, const uint16_t *x, double *out)
     }
 }
 
-void orc_row_bounds_f64(int32_t BH, int64_t L, int32_t bs, const uint8_t *mask, double scale,
+void orc_row_bounds_f64(int32_t BH, int64_t Lq, int64_t Lkv, int32_t bs, const uint8_t *mask, double scale,
                         const double *qnorm, const double *knorm, double *bound) {
-    const int32_t nb = (int32_t)(L / bs);
+    const int32_t nbkv = (int32_t)(Lkv / bs);
     for (int32_t bh = 0; bh < BH; ++bh)
-        for (int64_t i = 0; i < L; ++i) {
+        for (int64_t i = 0; i < Lq; ++i) {
             const int32_t qb = (int32_t)(i / bs);
             double kmax = 0.0;
             int any = 0;
-            for (int32_t kb = 0; kb < nb; ++kb) {
-                if (!mask[(int64_t)qb * nb + kb]) continue;
+            for (int32_t kb = 0; kb < nbkv; ++kb) {
+                if (!mask[(int64_t)qb * nbkv + kb]) continue;
                 for (int64_t j = (int64_t)kb * bs; j < (int64_t)(kb + 1) * bs; ++j) {
-                    const double kn = knorm[(int64_t)bh * L + j];
+                    const double kn = knorm[(int64_t)bh * Lkv + j];
                     if (!any || kn > kmax) kmax = kn;
                     any = 1;
                 }
             }
-            bound[(int64_t)bh * L + i] = scale * qnorm[(int64_t)bh * L + i] * kmax;
+            bound[(int64_t)bh * Lq + i] = scale * qnorm[(int64_t)bh * Lq + i] * kmax;
         }
 }
 
@@ -260,20 +264,20 @@ void orc_block_max_f32(int32_t BH, int32_t nb, int32_t bs, const float *knorm, f
         }
 }
 
-void orc_row_bounds_f32(int32_t BH, int64_t L, int32_t bs, const uint8_t *mask, float scale,
+void orc_row_bounds_f32(int32_t BH, int64_t Lq, int32_t nbkv, int32_t bs, const uint8_t *mask, float scale,
                         const float *qnorm, const float *kmax, float *rowbound) {
-    const int32_t nb = (int32_t)(L / bs);
+    const int32_t nbq = (int32_t)(Lq / bs);
     for (int32_t bh = 0; bh < BH; ++bh)
-        for (int32_t qb = 0; qb < nb; ++qb) {
+        for (int32_t qb = 0; qb < nbq; ++qb) {
             float kB = 0.0f;
-            for (int32_t kb = 0; kb < nb; ++kb)
-                if (mask[(int64_t)qb * nb + kb]) {
-                    const float m = kmax[(int64_t)bh * nb + kb];
+            for (int32_t kb = 0; kb < nbkv; ++kb)
+                if (mask[(int64_t)qb * nbkv + kb]) {
+                    const float m = kmax[(int64_t)bh * nbkv + kb];
                     kB = m > kB ? m : kB;
                 }
             for (int64_t i = (int64_t)qb * bs; i < (int64_t)(qb + 1) * bs; ++i) {
-                const float a = scale * qnorm[(int64_t)bh * L + i];
-                rowbound[(int64_t)bh * L + i] = a * kB;
+                const float a = scale * qnorm[(int64_t)bh * Lq + i];
+                rowbound[(int64_t)bh * Lq + i] = a * kB;
             }
         }
 }

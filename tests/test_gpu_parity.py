@@ -39,10 +39,11 @@ def _host_bf16(t):
 
 def run_gpu(ba, q, k, v, mask, bs, scale, flags=0, want_meta=True, lay=None):
     B, H, L, D = q.shape
-    nb = L // bs
+    L_kv = k.shape[2]
+    nb = L_kv // bs  # key blocks (kmax)
     own = lay is None
     if own:
-        lay = ba.bsattn_create_layout(B, H, L, D, bs, mask)
+        lay = ba.bsattn_create_layout(B, H, L, D, bs, mask, L_kv=L_kv)
     dq, dk, dv = _dev(q), _dev(k), _dev(v)
     o = torch.full_like(dq, float("nan"))
     qn = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
@@ -106,7 +107,7 @@ def full_case(ba, q, k, v, mask, bs, scale, flags=0, what=""):
 # ------------------------------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("name", ["tiny", "small"])
+@pytest.mark.parametrize("name", ["tiny", "small", "stream_small"])
 def test_workload_full(ba, name):
     w = synth.WORKLOADS[name]
     q, k, v = synth.make_qkv(w)
@@ -232,6 +233,22 @@ def test_guard_fires_on_eligible_rows(ba):
     assert must <= res["fb_rows"] <= may and res["fb_units"] >= 1
 
 
+def test_streamed_chunk_equals_last_rows_of_the_full_window(ba):
+    # the chunk's queries are the last query rows of the full-window problem and its mask the
+    # last mask rows, and every row's key tiles are the same: the GPU rows must be identical
+    w = synth.WORKLOADS["stream_small"]
+    wf = synth.Workload("full", w.B, w.H, w.D, w.frames, w.block, w.mask, w.keys, w.seed)
+    q, k, v = synth.make_qkv(w)
+    qf, _, _ = synth.make_qkv(wf)
+    chunk = run_gpu(ba, q, k, v, w.block_mask(), w.block, w.scale)
+    full = run_gpu(ba, qf, k, v, wf.block_mask(), w.block, w.scale)
+    tail = full["o_raw"][:, :, w.L_kv - w.L:]
+    assert torch.equal(chunk["o_raw"].view(torch.int16), tail.contiguous().view(torch.int16))
+    assert np.array_equal(chunk["kmax"].view(np.uint32), full["kmax"].view(np.uint32))
+    assert np.array_equal(chunk["rowbound"].view(np.uint32),
+                          full["rowbound"][:, :, w.L_kv - w.L:].view(np.uint32))
+
+
 def test_deterministic(ba):
     w = synth.WORKLOADS["small"]
     q, k, v = synth.make_qkv(w)
@@ -240,7 +257,8 @@ def test_deterministic(ba):
     assert torch.equal(a["o_raw"].view(torch.int16), b["o_raw"].view(torch.int16))
 
 
-@pytest.mark.parametrize("name,heads", [("720p", [0, 7, 23]), ("stress", [0, 11]), ("1080p", [5])])
+@pytest.mark.parametrize("name,heads", [("720p", [0, 7, 23]), ("stress", [0, 11]), ("1080p", [5]),
+                                        ("stream", [0, 13])])
 def test_workload_sampled(ba, name, heads):
     w = synth.WORKLOADS[name]
     q, k, v = synth.make_qkv(w)
@@ -276,7 +294,8 @@ def _pinned(x):
     return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
 
 
-@pytest.mark.parametrize("name,pairs,flags", [("small", 3, 0), ("small", 0, 1), ("tiny", 1, 4)])
+@pytest.mark.parametrize("name,pairs,flags", [("small", 3, 0), ("small", 0, 1), ("tiny", 1, 4),
+                                              ("stream_small", 3, 0)])
 def test_host_path_equals_device_path(ba, name, pairs, flags):
     # bsattn_forward_host (pinned host tensors, chunked copies and kernels on three streams)
     # against bsattn_forward on device copies: the same kernels per row, so identical bits.
@@ -286,7 +305,7 @@ def test_host_path_equals_device_path(ba, name, pairs, flags):
     if name == "tiny":  # a loose key, so the guard flags rows (bound softmax for every row)
         q, k, v = _scaled_key(w, 1e4)
     mask = w.block_mask()
-    lay = ba.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask)
+    lay = ba.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, L_kv=w.L_kv)
     dev = run_gpu(ba, q, k, v, mask, w.block, w.scale, flags, want_meta=False, lay=lay)
     hq, hk, hv = _pinned(q), _pinned(k), _pinned(v)
     ho = torch.full_like(hq, float("nan")).pin_memory()

@@ -38,11 +38,11 @@ def check_tiles(mask, bs, tile_ptr, tiles):
     """Key tiles of each query frame: exactly its allowed keys, in order; widths a multiple
     of 16 and at most 128; a tile never spans a masked frame; within a run of consecutive
     allowed frames every tile but the last is 128 keys."""
-    nb = mask.shape[0]
+    nb, nbkv = mask.shape
     for qb in range(nb):
         t = tiles[tile_ptr[qb]:tile_ptr[qb + 1]]
         keys = np.concatenate([np.arange(s, s + w) for s, w in t]) if len(t) else np.zeros(0, int)
-        allowed = np.concatenate([np.arange(kb * bs, (kb + 1) * bs) for kb in range(nb) if mask[qb, kb]]
+        allowed = np.concatenate([np.arange(kb * bs, (kb + 1) * bs) for kb in range(nbkv) if mask[qb, kb]]
                                  ) if mask[qb].any() else np.zeros(0, int)
         assert np.array_equal(keys, allowed)
         assert np.all(t[:, 1] % 16 == 0) and np.all((t[:, 1] >= 16) & (t[:, 1] <= 128))
@@ -55,12 +55,13 @@ def check_tiles(mask, bs, tile_ptr, tiles):
 def test_plan_matches_oracle(lib, name):
     w = synth.WORKLOADS[name]
     mask = w.block_mask()
-    lay = bsattn.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, bsattn.BSATTN_PLAN_ONLY)
+    lay = bsattn.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, bsattn.BSATTN_PLAN_ONLY, L_kv=w.L_kv)
     info = lay.info
     row_ptr, col_idx, units, tile_ptr, tiles = bsattn.bsattn_layout_export(lay, with_tiles=True)
     orp, oci = oracle.allowed_csr(mask)
     assert np.array_equal(row_ptr, orp) and np.array_equal(col_idx, oci)
     assert info.nnz_blocks == len(oci) and info.nb == w.nb
+    assert info.L == w.L and info.L_kv == w.L_kv and info.nb_kv == w.nb_kv
     assert info.kv_tile == 128 and info.key_tiles == len(tiles)
     check_tiles(mask, w.block, tile_ptr, tiles)
     nqt = -(-w.block // 128)
@@ -107,6 +108,17 @@ def test_create_rejects_bad_arguments(lib, args, status):
     mask = np.ones((min(nb, 5000), min(nb, 5000)), np.uint8)
     st, lay = bsattn.bsattn_create_layout(B, H, L, D, bs, mask, bsattn.BSATTN_PLAN_ONLY, raise_on_error=False)
     assert st == status and lay is None
+
+
+def test_rect_create_checks_the_key_side(lib):
+    mask = np.ones((2, 5), np.uint8)
+    st, lay = bsattn.bsattn_create_layout(1, 1, 32, 64, 16, mask, bsattn.BSATTN_PLAN_ONLY, raise_on_error=False,
+                                          L_kv=88)  # 88 keys: not a multiple of the block
+    assert st == bsattn.BSATTN_ERR_UNALIGNED_BLOCK and lay is None
+    lay = bsattn.bsattn_create_layout(1, 1, 32, 64, 16, mask, bsattn.BSATTN_PLAN_ONLY, L_kv=80)
+    assert (lay.info.nb, lay.info.nb_kv, lay.info.L, lay.info.L_kv) == (2, 5, 32, 80)
+    assert lay.info.nnz_blocks == 10
+    lay.destroy()
 
 
 def test_create_rejects_null_mask_and_bad_flags(lib):

@@ -32,11 +32,12 @@ def _rand_qkv(B, H, L, D, seed=7):
 
 
 def _brute_dense(q, k, v, mask, bs, scale):
-    """Dense route: full S = scale Q K^T over every key, element mask from the block mask."""
+    """Dense route: full S = scale Q K^T over every key, element mask from the block mask
+    (q [B,H,Lq,D], k and v [B,H,Lkv,D], mask [Lq/bs, Lkv/bs])."""
     qf, kf, vf = _f64(q), _f64(k), _f64(v)
     B, H, L, D = qf.shape
-    blk = np.arange(L) // bs
-    allowed = mask.astype(bool)[blk[:, None], blk[None, :]]  # [L, L]
+    Lkv = kf.shape[2]
+    allowed = mask.astype(bool)[(np.arange(L) // bs)[:, None], (np.arange(Lkv) // bs)[None, :]]  # [Lq, Lkv]
     O = np.zeros((B, H, L, D))
     LSE = np.full((B, H, L), -np.inf)
     for b in range(B):
@@ -65,6 +66,71 @@ def test_brute_force_dense_tiny(name):
     Ob, lseb = _brute_dense(q, k, v, w.block_mask(), w.block, w.scale)
     assert np.max(np.abs(O - Ob)) <= 1e-12
     assert np.max(np.abs(lse - lseb)) <= 1e-12
+
+
+def test_brute_force_streamed_chunk():
+    # queries of a 3-frame chunk reading 4 context frames plus the chunk (7 key frames), with a
+    # rectangular mask that is not a slice of any symmetric rule, and one query frame reading nothing
+    B, H, D, bs, nq, nkv = 2, 2, 64, 16, 3, 7
+    mask = np.zeros((nq, nkv), np.uint8)
+    mask[0, [0, 3, 4]] = 1
+    mask[1, [0, 1, 5, 6]] = 1
+    q = synth.tensor_bf16(11, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(11, synth.TAG_K, B, H, nkv * bs, D)
+    v = synth.tensor_bf16(11, synth.TAG_V, B, H, nkv * bs, D)
+    scale = float(np.float32(1 / 8))
+    O, lse, _ = oracle.attention(q, k, v, mask, bs, scale)
+    Ob, lseb = _brute_dense(q, k, v, mask, bs, scale)
+    assert np.max(np.abs(O - Ob)) <= 1e-12
+    fin = np.isfinite(lseb)
+    assert np.array_equal(np.isfinite(lse), fin) and np.max(np.abs(lse[fin] - lseb[fin])) <= 1e-12
+    # the frame that reads nothing: O = 0
+    rows = (np.arange(B * H * nq * bs) % (nq * bs)) // bs == 2
+    assert np.all(O[rows] == 0)
+
+
+def test_streamed_chunk_equals_last_rows_of_the_full_window():
+    # a chunk's queries are the last query rows of the self-attention problem over all frames, and
+    # its mask the last rows of that problem's mask: the outputs must be the same rows
+    w = synth.WORKLOADS["stream_small"]
+    wf = synth.Workload("full", w.B, w.H, w.D, w.frames, w.block, w.mask, w.keys, w.seed)
+    q, k, v = synth.make_qkv(w)
+    qf, kf, vf = synth.make_qkv(wf)
+    assert np.array_equal(k, kf) and np.array_equal(q, qf[:, :, w.L_kv - w.L:])
+    rows = np.array([0, 57, 399, 400, 1199], dtype=np.int64)
+    O, lse, _ = oracle.attention(q, k, v, w.block_mask(), w.block, w.scale, rows=rows)
+    Of, lsef, _ = oracle.attention(qf, kf, vf, wf.block_mask(), w.block, w.scale, rows=rows + (w.L_kv - w.L))
+    assert np.array_equal(O, Of) and np.array_equal(lse, lsef)
+
+
+def test_sdpa_streamed_all_ones():
+    # every chunk query reads every key: torch's fp64 scaled_dot_product_attention with Lq != Lkv
+    B, H, D, bs, nq, nkv = 1, 2, 64, 16, 2, 5
+    q = synth.tensor_bf16(5, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(5, synth.TAG_K, B, H, nkv * bs, D)
+    v = synth.tensor_bf16(5, synth.TAG_V, B, H, nkv * bs, D)
+    scale = 0.125
+    O, _, _ = oracle.attention(q, k, v, np.ones((nq, nkv), np.uint8), bs, scale)
+    t = [torch.from_numpy(_f64(x)) for x in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*t, scale=scale).numpy().reshape(-1, D)
+    assert np.max(np.abs(O - ref)) <= 1e-12
+
+
+def test_streamed_metadata_bounds_and_cauchy_schwarz():
+    # rectangular metadata: fp32 recipe against fp64 norms; every unmasked logit below its bound
+    B, H, D, bs, nq, nkv = 1, 2, 64, 16, 2, 5
+    mask = synth.window_mask(nkv, 1, True)[nkv - nq:]
+    q = synth.tensor_bf16(9, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(9, synth.TAG_K, B, H, nkv * bs, D)
+    qn, km, rb = oracle.metadata_f32(q, k, mask, bs, 0.125)
+    assert km.shape == (B, H, nkv) and rb.shape == (B, H, nq * bs)
+    M = oracle.row_bounds_f64(oracle.row_norms_f64(q), oracle.row_norms_f64(k), mask, bs, 0.125)
+    assert np.max(np.abs(rb - M) / M) <= 2.0 ** -20
+    qf, kf = _f64(q), _f64(k)
+    for h in range(H):
+        S = 0.125 * qf[0, h] @ kf[0, h].T
+        allowed = mask.astype(bool)[(np.arange(nq * bs) // bs)[:, None], (np.arange(nkv * bs) // bs)[None, :]]
+        assert np.all(S[allowed] <= np.broadcast_to(M[0, h][:, None], S.shape)[allowed])
 
 
 def test_brute_force_asymmetric_mask():
@@ -287,6 +353,7 @@ def test_workload_sizes_golden():
         assert len(col_idx) == g[name]["nnz"], name
         assert (w.B, w.H, w.D, w.frames, w.block) == (g[name]["B"], g[name]["H"], g[name]["D"],
                                                        g[name]["frames"], g[name]["block"])
+        assert w.nq == g[name].get("q_frames", g[name]["frames"])
         assert synth.useful_flop(w) == g[name]["useful_flop"]
         # ascending within each query block
         for qb in range(w.nb):
