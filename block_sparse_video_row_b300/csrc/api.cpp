@@ -62,6 +62,9 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
         lay.tile_ptr[qb + 1] = static_cast<int32_t>(lay.tiles.size() / 2);
     }
 
+    // Cost model (in hundredths of a two-tile key tile): a unit of two query tiles takes
+    // 100 per key tile; a unit of one tile 83, because its softmax cannot overlap another
+    // tile's MMAs; plus 150 per unit (query loads, epilogue).
     struct Unit {
         int32_t bh, qb, qt0, nt;
         int64_t cost;
@@ -71,12 +74,10 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     us.reserve(static_cast<size_t>(BH) * nb * ((lay.qt_per_block + 1) / 2));
     for (int32_t bh = 0; bh < BH; ++bh)
         for (int32_t qb = 0; qb < nb; ++qb) {
-            const int64_t keys = static_cast<int64_t>(lay.row_ptr[qb + 1] - lay.row_ptr[qb]) * lay.bs;
             const int64_t ntile = lay.tile_ptr[qb + 1] - lay.tile_ptr[qb];
             for (int32_t qt0 = 0; qt0 < lay.qt_per_block; qt0 += 2) {
                 const int32_t nt = std::min(2, lay.qt_per_block - qt0);
-                // cost ~ MMA work (keys) plus a per-tile pipeline overhead
-                us.push_back({bh, qb, qt0, nt, (keys + 32 * ntile) * nt});
+                us.push_back({bh, qb, qt0, nt, ntile * (nt == 2 ? 100 : 83) + 150});
             }
         }
     // Largest first (longest-processing-time order for the persistent CTAs); equal
@@ -84,11 +85,13 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     std::stable_sort(us.begin(), us.end(), [](const Unit &a, const Unit &b) { return a.cost > b.cost; });
     lay.n_units = static_cast<int32_t>(us.size());
     lay.units.resize(us.size() * 4);
+    lay.unit_cost.resize(us.size());
     for (size_t i = 0; i < us.size(); ++i) {
         lay.units[4 * i + 0] = us[i].bh;
         lay.units[4 * i + 1] = us[i].qb;
         lay.units[4 * i + 2] = us[i].qt0;
         lay.units[4 * i + 3] = us[i].nt;
+        lay.unit_cost[i] = us[i].cost;
     }
     int64_t reading_frames = 0;
     for (int32_t qb = 0; qb < nb; ++qb) reading_frames += lay.row_ptr[qb + 1] > lay.row_ptr[qb] ? 1 : 0;
@@ -171,12 +174,15 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
 
     const size_t nnz = std::max<size_t>(lay.col_idx.size(), 1);
     const size_t ntiles = std::max<size_t>(lay.tiles.size() / 2, 1);
-    const size_t ws_ints = kWsHeader + 2 * static_cast<size_t>(lay.n_units);
+    lay.grid = std::max(1, std::min(lay.n_units, lay.num_sms));
+    std::vector<int32_t> slots;
+    lay.n_slots = bsv::schedule_units(lay, lay.grid, slots);
+    const size_t ws_ints = kWsHeader + 2 * static_cast<size_t>(lay.n_slots);
     if ((e = cudaMalloc(&lay.d_row_ptr, lay.row_ptr.size() * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_col_idx, nnz * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_tile_ptr, lay.tile_ptr.size() * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_tiles, ntiles * sizeof(int2))) != cudaSuccess ||
-        (e = cudaMalloc(&lay.d_units, static_cast<size_t>(lay.n_units) * sizeof(int4))) != cudaSuccess ||
+        (e = cudaMalloc(&lay.d_units, static_cast<size_t>(lay.n_slots) * sizeof(int4))) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_ws, ws_ints * 4)) != cudaSuccess) {
         free_device(&lay);
         return from_cuda(e);
@@ -186,7 +192,7 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
         (!lay.col_idx.empty() &&
          (e = cudaMemcpy(lay.d_col_idx, lay.col_idx.data(), lay.col_idx.size() * 4, cudaMemcpyHostToDevice)) !=
              cudaSuccess) ||
-        (e = cudaMemcpy(lay.d_units, lay.units.data(), lay.units.size() * 4, cudaMemcpyHostToDevice)) !=
+        (e = cudaMemcpy(lay.d_units, slots.data(), slots.size() * 4, cudaMemcpyHostToDevice)) !=
             cudaSuccess ||
         (e = cudaMemcpy(lay.d_tile_ptr, lay.tile_ptr.data(), lay.tile_ptr.size() * 4, cudaMemcpyHostToDevice)) !=
             cudaSuccess ||
@@ -201,7 +207,7 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
     lay.ws.fb_count = lay.d_ws + 4;
     lay.ws.fb_rows = lay.d_ws + 5;
     lay.ws.unit_flag = lay.d_ws + kWsHeader;
-    lay.ws.fb_list = lay.d_ws + kWsHeader + lay.n_units;
+    lay.ws.fb_list = lay.d_ws + kWsHeader + lay.n_slots;
 
     uint64_t ms = 4000;
     if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
@@ -222,6 +228,33 @@ bsattn_status check_runnable(const bsattn_layout_s *lay) {
 }  // namespace
 
 namespace bsv {
+int32_t schedule_units(const bsattn_layout_s &lay, int32_t G, std::vector<int32_t> &slots) {
+    G = std::max(1, G);
+    std::vector<std::vector<int32_t>> per(static_cast<size_t>(G));
+    std::vector<int64_t> load(static_cast<size_t>(G), 0);
+    // least-loaded CTA first (ties: lowest index), units in cost order
+    typedef std::pair<int64_t, int32_t> Entry;
+    std::vector<Entry> heap;
+    for (int32_t c = 0; c < G; ++c) heap.push_back({0, c});
+    auto cmp = [](const Entry &a, const Entry &b) { return a.first != b.first ? a.first > b.first : a.second > b.second; };
+    std::make_heap(heap.begin(), heap.end(), cmp);
+    for (int32_t u = 0; u < lay.n_units; ++u) {
+        std::pop_heap(heap.begin(), heap.end(), cmp);
+        Entry &e = heap.back();
+        per[e.second].push_back(u);
+        e.first += lay.unit_cost[u];
+        std::push_heap(heap.begin(), heap.end(), cmp);
+    }
+    size_t K = 0;
+    for (const auto &v : per) K = std::max(K, v.size());
+    slots.assign(K * G * 4, 0);
+    for (size_t k = 0; k < K; ++k)
+        for (int32_t c = 0; c < G; ++c)
+            if (k < per[c].size())
+                for (int f = 0; f < 4; ++f) slots[(k * G + c) * 4 + f] = lay.units[4 * per[c][k] + f];
+    return static_cast<int32_t>(K * G);
+}
+
 bool encode_layout_maps(const bsattn_layout_s *lay, const void *q, const void *k, const void *v, CUtensorMap *tq,
                         CUtensorMap *tk, CUtensorMap *tv) {
     return encode_fn() && encode_q_map(tq, *lay, q) && encode_kv_map(tk, *lay, k) && encode_kv_map(tv, *lay, v);
@@ -326,12 +359,12 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
         return BSATTN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // per-call part of the workspace: fb_count, fb_rows and the unit flags
-    cudaError_t e = cudaMemsetAsync(lay->d_ws + 4, 0, (kWsHeader - 4 + static_cast<size_t>(lay->n_units)) * 4, s);
+    cudaError_t e = cudaMemsetAsync(lay->d_ws + 4, 0, (kWsHeader - 4 + static_cast<size_t>(lay->n_slots)) * 4, s);
     if (e != cudaSuccess) return from_cuda(e);
 
     bsv::AttnParams p;
     p.units = lay->d_units;
-    p.n_units = lay->n_units;
+    p.n_units = lay->n_slots;
     p.tile_ptr = lay->d_tile_ptr;
     p.tiles = lay->d_tiles;
     p.rowbound = rowbound;
@@ -346,7 +379,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
     p.debug_stall = (flags & BSATTN_DEBUG_STALL) ? 1 : 0;
     p.timeout_ns = lay->timeout_ns;
-    const int grid = std::max(1, std::min(lay->n_units, lay->num_sms));
+    const int grid = lay->grid;  // the width the schedule was built for
     auto launch = [&](bool on) {
         return lay->D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, on, grid, s)
                              : bsv::launch_attention_d64(tq, tk, tv, p, on, grid, s);

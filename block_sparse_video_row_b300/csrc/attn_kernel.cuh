@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 const int4 U = p.units[unit_index(p, i)];
                 const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
-                if (nkv == 0) continue;
+                if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
                 // testing only: the first unit's query tiles are never loaded, so the
                 // issuers' bounded waits run out and the CTA aborts and returns
                 const int n_q = (p.debug_stall && i == static_cast<int>(blockIdx.x)) ? 0 : U.w;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 const int4 U = p.units[unit_index(p, i)];
                 const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
-                if (nkv == 0) continue;
+                if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
                 if (t >= U.w) {
                     // This query tile is absent from the unit: release each stage without MMAs,
                     // after its copy has landed (so the arrival counts toward the right phase).
@@ -514,6 +514,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int u = unit_index(p, i);
             const int4 U = p.units[u];
             const int nt = U.w;
+            if (nt == 0) continue;  // an empty schedule slot
             const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
             const int64_t row0 = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
                                  static_cast<int64_t>(U.z) * kQTile + r;  // this thread's row of tile 0

@@ -6,10 +6,17 @@
 
 #include "internal.h"
 
+struct bsattn_layout_s;
+
 namespace bsv {
 struct HostPipe;                   // staging and streams of bsattn_forward_host (host_pipeline.cu)
 void host_pipe_destroy(HostPipe *hp);
 constexpr int kWsHeader = 8;       // int32 workspace slots: [0] status, [4] fb_count, [5] fb_rows
+// The per-CTA schedule for a grid of G persistent CTAs: the units, in the layout's
+// cost order, each given to the least-loaded CTA; slot k * G + c holds CTA c's k-th
+// unit (4 int32 each), and empty slots are (0, 0, 0, 0), a unit of no query tiles
+// that every role skips.  Returns the number of slots (a multiple of G).
+int32_t schedule_units(const bsattn_layout_s &lay, int32_t G, std::vector<int32_t> &slots);
 }  // namespace bsv
 
 struct bsattn_layout_s {
@@ -21,6 +28,8 @@ struct bsattn_layout_s {
     std::vector<int32_t> row_ptr, col_idx, units;
     std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs
     int32_t kv_tile = 0, qt_per_block = 0, n_units = 0;
+    std::vector<int64_t> unit_cost;  // cost model of each unit of `units`
+    int32_t grid = 0, n_slots = 0;   // persistent CTAs and scheduled slots (device layouts)
     int64_t mma_rows = 0;
     double useful_flop = 0.0;
     int device = -1, num_sms = 0;

@@ -127,7 +127,10 @@ enum {
  * an exactly sized MMA with no element mask or padding and none reaches into a
  * masked frame); query tiles of 128 rows that never straddle a frame edge (the
  * last tile of a frame may be partial); and a work list of pairs of query
- * tiles of one frame, sorted by cost, largest first.
+ * tiles of one frame, sorted by cost, largest first (cost: 100 per key tile
+ * for a unit of two query tiles, 83 for one tile, whose softmax cannot overlap
+ * another tile's MMAs, plus 150 per unit).  A device layout deals the units to
+ * its persistent CTAs (one per SM) by that cost, each to the least-loaded CTA.
  * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA, OOM or DEVICE.
  */
 bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,

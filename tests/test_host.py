@@ -73,9 +73,10 @@ def test_plan_matches_oracle(lib, name):
         assert nt in (1, 2) and qt0 % 2 == 0 and qt0 + nt <= nqt
         seen[bh, qb, qt0:qt0 + nt] += 1
     assert np.all(seen == 1)
-    # largest cost first
-    keys = np.diff(orp)[units[:, 1]] * w.block + 32 * np.diff(tile_ptr)[units[:, 1]]
-    cost = keys * units[:, 3]
+    # largest cost first, by the documented model: 100 per key tile for a unit of two query
+    # tiles, 83 for one tile, plus 150 per unit
+    ntile = np.diff(tile_ptr)[units[:, 1]]
+    cost = ntile * np.where(units[:, 3] == 2, 100, 83) + 150
     assert np.all(np.diff(cost) <= 0)
     lay.destroy()
 
