@@ -278,6 +278,7 @@ bsattn_status bsattn_create_layout_rect(bsattn_layout_t *out, int32_t B, int32_t
     if (block_size % 16 != 0 || L % block_size != 0 || L_kv % block_size != 0) return BSATTN_ERR_UNALIGNED_BLOCK;
     const int64_t nb = L / block_size, nbkv = L_kv / block_size;
     if (nb > BSATTN_MAX_NB || nbkv > BSATTN_MAX_NB) return BSATTN_ERR_UNSUPPORTED;
+    if (L_kv < L) return BSATTN_ERR_UNSUPPORTED;  // a chunk reads at least its own frames' worth of keys
     if (static_cast<int64_t>(B) * H * std::max(L, L_kv) > BSATTN_MAX_ROWS) return BSATTN_ERR_UNSUPPORTED;
 
     bsattn_layout_s *lay = new (std::nothrow) bsattn_layout_s;

@@ -57,48 +57,50 @@ __device__ __forceinline__ float tree16(float s, unsigned mask) {
     return s;
 }
 
-// One CTA per (row chunk of one block) of Q (the first BH * nb * chunks CTAs) or of K
-// (the rest): Q chunks write their rows' norms, K chunks fold theirs into the block's max.
+// One CTA per row chunk of one key block kb: it folds the chunk's key norms into
+// kmax[b, h, kb] and, when query block kb exists (kb < nb; a streamed chunk has
+// fewer query than key blocks), writes the norms of the same rows of Q.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) norms_kernel(const BoundsParams p) {
     constexpr int PER = D / 16;
     const int cpb = p.chunks_per_block;
-    const int64_t q_ctas = static_cast<int64_t>(p.BH) * p.nb * cpb;
-    const bool is_q = static_cast<int64_t>(blockIdx.x) < q_ctas;
-    const int64_t id = is_q ? blockIdx.x : blockIdx.x - q_ctas;
-    const int nblk = is_q ? p.nb : p.nbkv;
-    const int64_t L = is_q ? p.L : p.Lkv;
-    const int chunk = static_cast<int>(id % cpb);
-    const int64_t seg = id / cpb;  // (b*H + h) * nblk + blk
-    const int blk = static_cast<int>(seg % nblk);
-    const int64_t bh = seg / nblk;
-    const int64_t row0 = bh * L + static_cast<int64_t>(blk) * p.block + static_cast<int64_t>(chunk) * kChunkRows;
+    const int chunk = static_cast<int>(blockIdx.x % cpb);
+    const int64_t seg = blockIdx.x / cpb;  // (b*H + h) * nbkv + kb
+    const int kb = static_cast<int>(seg % p.nbkv);
+    const int64_t bh = seg / p.nbkv;
+    const bool has_q = kb < p.nb;
+    const int64_t in_blk = static_cast<int64_t>(kb) * p.block + static_cast<int64_t>(chunk) * kChunkRows;
+    const int64_t krow0 = bh * p.Lkv + in_blk;
+    const int64_t qrow0 = bh * p.L + in_blk;
     const int nrows = min(kChunkRows, p.block - chunk * kChunkRows);  // a multiple of 16
-    const uint16_t *x = is_q ? p.q : p.k;
     const int lane16 = threadIdx.x & 15;
     const int grp = threadIdx.x >> 4;
     const unsigned gmask = 0xFFFFu << (threadIdx.x & 16);
 
     float kmax = 0.0f;
-    constexpr int U = 8;  // rows per group in flight
+    constexpr int U = 4;  // rows per group in flight
     for (int r = grp; r < nrows; r += 16 * U) {
-        uint32_t w[U][PER / 2];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (r + 16 * u < nrows) load_chunk<PER>(x + (row0 + r + 16 * u) * D + lane16 * PER, w[u]);
+        uint32_t wq[U][PER / 2], wk[U][PER / 2];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (r + 16 * u < nrows) {
-                const float n = __fsqrt_rn(tree16(chunk_sumsq<PER>(w[u]), gmask));
-                if (is_q) {
-                    if (lane16 == 0) p.qnorm[row0 + r + 16 * u] = n;
-                } else {
-                    kmax = n > kmax ? n : kmax;
+                const int64_t off = static_cast<int64_t>(r + 16 * u) * D + lane16 * PER;
+                if (has_q) load_chunk<PER>(p.q + qrow0 * D + off, wq[u]);
+                load_chunk<PER>(p.k + krow0 * D + off, wk[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (r + 16 * u < nrows) {
+                if (has_q) {
+                    const float qn = __fsqrt_rn(tree16(chunk_sumsq<PER>(wq[u]), gmask));
+                    if (lane16 == 0) p.qnorm[qrow0 + r + 16 * u] = qn;
                 }
+                const float kn = __fsqrt_rn(tree16(chunk_sumsq<PER>(wk[u]), gmask));
+                kmax = kn > kmax ? kn : kmax;
             }
         }
     }
-    if (is_q) return;  // uniform per CTA
     // CTA max of the key norms, then one atomic per CTA (norms are >= 0, so the
     // unsigned order of the fp32 bit patterns is the numeric order).
 #pragma unroll
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsPara
 }
 
 cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s) {
-    const int64_t grid = static_cast<int64_t>(p.BH) * (p.nb + p.nbkv) * p.chunks_per_block;
+    const int64_t grid = static_cast<int64_t>(p.BH) * p.nbkv * p.chunks_per_block;  // nb <= nbkv
     if (D == 128)
         norms_kernel<128><<<static_cast<unsigned>(grid), kNormThreads, 0, s>>>(p);
     else

@@ -137,8 +137,8 @@ bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, i
                                    int32_t block_size, const uint8_t *block_mask, int32_t flags);
 
 /*
- * The same for a streamed chunk: L query tokens (the chunk) reading L_kv key
- * tokens (context frames and the chunk).  block_mask is nb * nb_kv bytes,
+ * The same for a streamed chunk: L query tokens (the chunk) reading L_kv >= L key
+ * tokens (context frames and the chunk; L_kv < L returns BSATTN_ERR_UNSUPPORTED).  block_mask is nb * nb_kv bytes,
  * nb = L / block_size, nb_kv = L_kv / block_size, row-major by query block.
  * Q and O are [B, H, L, D], K and V [B, H, L_kv, D], qnorm and rowbound
  * [B, H, L], kmax [B, H, nb_kv].  bsattn_create_layout(..., L, ...) equals

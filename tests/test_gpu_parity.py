@@ -147,6 +147,24 @@ def test_edge_shapes(ba, D, B, H, frames, bs, mask_kind):
 
 # online max everywhere; bound without the rerun; bound for every row (no eligibility switch),
 # with and without the rerun
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B,H,nq,nkv,bs", [
+    (2, 3, 1, 3, 48),     # one query frame reading three key frames; partial query tile
+    (1, 2, 2, 2, 16),     # L_kv == L through the rectangular entry point
+    (1, 2, 3, 9, 272),    # three query tiles per frame, 16-row tail, irregular mask
+])
+def test_streamed_edge_shapes(ba, D, B, H, nq, nkv, bs):
+    rng = np.random.default_rng(nq * 100 + nkv)
+    mask = (rng.random((nq, nkv)) < 0.6).astype(np.uint8)
+    mask[:, 0] = 1                       # every query frame reads at least the first key frame
+    mask[np.arange(nq), nkv - nq + np.arange(nq)] = 1  # and its own frame
+    q = synth.tensor_bf16(4, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(4, synth.TAG_K, B, H, nkv * bs, D)
+    v = synth.tensor_bf16(4, synth.TAG_V, B, H, nkv * bs, D)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    full_case(ba, q, k, v, mask, bs, scale, what=f"stream {B}x{H} {nq}/{nkv}x{bs} D{D}")
+
+
 @pytest.mark.parametrize("flags", [1, 2, 4, 6])
 def test_variants_small(ba, flags):
     w = synth.WORKLOADS["small"]

@@ -116,6 +116,9 @@ def test_rect_create_checks_the_key_side(lib):
     st, lay = bsattn.bsattn_create_layout(1, 1, 32, 64, 16, mask, bsattn.BSATTN_PLAN_ONLY, raise_on_error=False,
                                           L_kv=88)  # 88 keys: not a multiple of the block
     assert st == bsattn.BSATTN_ERR_UNALIGNED_BLOCK and lay is None
+    st, lay = bsattn.bsattn_create_layout(1, 1, 96, 64, 16, np.ones((6, 5), np.uint8), bsattn.BSATTN_PLAN_ONLY,
+                                          raise_on_error=False, L_kv=80)  # more query than key tokens
+    assert st == bsattn.BSATTN_ERR_UNSUPPORTED and lay is None
     lay = bsattn.bsattn_create_layout(1, 1, 32, 64, 16, mask, bsattn.BSATTN_PLAN_ONLY, L_kv=80)
     assert (lay.info.nb, lay.info.nb_kv, lay.info.L, lay.info.L_kv) == (2, 5, 32, 80)
     assert lay.info.nnz_blocks == 10
