@@ -16,7 +16,10 @@
 //
 // One CTA per SM processes work units: a unit is one or two 128-row query tiles
 // of the same frame (they share every K/V tile), looping over the frame's key
-// tiles.
+// tiles.  The host deals the units to the CTAs (slot k * gridDim + c is CTA c's
+// k-th unit; empty slots have no query tiles and are skipped).  Query rows index
+// Q and O over L tokens per head, keys index K and V over L_kv >= L (a streamed
+// chunk reads context frames before its own).
 //   warp 0      TMA producer: Q tiles, then a ring of STAGES K and V tiles.
 //   warps 1, 2  MMA issuers (one thread each), one per query tile t = warp - 1:
 //               S_t = Q_t K^T (A, B from smem) and O_t += P_t V (A = P_t from
@@ -30,11 +33,14 @@
 // P (bf16, two per 32-bit column) of key half h overwrites the first 32 of that
 // half's 64 S columns: keys 64h + 2c, 64h + 2c + 1 sit in column 64h + c.
 //
-// Issuer t issues, per key tile j, PV_t(j) then S_t(j+1).  tcgen05 MMAs from one
-// thread complete in issue order, so the commit that signals S_t(j+1) also
-// guarantees that PV_t(j) has finished: O_t is stable whenever its softmax holds
-// S_t (the online variant rescales it then).  Each K/V stage is released by both
-// issuers (a tile absent from a unit still takes part, without MMAs).
+// Issuer t issues, per key tile j, PV_t(j) then S_t(j+1).  PV_t(j) comes in two
+// parts: the k-steps of each half's first 32 keys once every softmax warp has
+// stored that P (p_full), the rest with S_t(j+1) once all of P is stored
+// (p_rest), so the first part overlaps the end of the softmax.  tcgen05 MMAs
+// from one thread complete in issue order, so the commit that signals S_t(j+1)
+// also guarantees that PV_t(j) has finished: O_t is stable whenever its softmax
+// holds S_t (the online variant rescales it then).  Each K/V stage is released by
+// both issuers (a tile absent from a unit still takes part, without MMAs).
 //
 // Every wait is bounded (a wall-clock limit, mbarriers only: no named barrier
 // inside the loops); on expiry the CTA raises a shared abort flag and a device
