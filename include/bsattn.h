@@ -15,10 +15,11 @@
  *    which holds by Cauchy-Schwarz, so exp(S - m_i) accumulates with no
  *    rescaling (deep-dive, section 拿掉 softmax 的序列相依 / "remove softmax's
  *    serial dependency"; "How is HeyGen optimizing AI video on Google Cloud
- *    TPUs", section "Innovating Beyond Serial Dependencies").  Rows where the
- *    bound is so loose that the exponentials underflow are detected and rerun
- *    with a running-max (online softmax) kernel (the deep-dive's per-head
- *    eligibility check with fallback to online softmax, same section).
+ *    TPUs", section "Innovating Beyond Serial Dependencies").  Following the
+ *    deep-dive's eligibility check with fallback to online softmax (same
+ *    section), rows whose bound is far above any plausible logit take the
+ *    running max in the same launch, and rows whose exponentials underflow
+ *    anyway are detected and rerun with a running-max (online softmax) kernel.
  *
  * Tensors: Q and O are bf16, contiguous [B, H, L, D] with L = nb * block_size;
  * K and V are [B, H, L_kv, D] with L_kv = nb_kv * block_size; 16-byte-aligned
@@ -55,6 +56,11 @@
 extern "C" {
 #endif
 
+/* Bounded waits: every wait inside the kernels gives up after a wall-clock limit
+ * (the environment variable BSATTN_TIMEOUT_MS, read when a layout is created;
+ * default 4000 ms), records BSATTN_ERR_TIMEOUT in the layout's status word and
+ * returns, so a stalled pipeline never hangs the GPU. */
+
 /* A cudaStream_t, passed through unchanged (NULL = the legacy default stream). */
 typedef struct CUstream_st *bsattn_stream_t;
 
@@ -68,7 +74,7 @@ typedef enum {
     BSATTN_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
     BSATTN_ERR_OOM = 5,             /* device allocation failed at create */
     BSATTN_ERR_TIMEOUT = 6,         /* a bounded device wait ran out (reported by query_stats) */
-    BSATTN_ERR_DEVICE = 7           /* no usable sm_100-family device */
+    BSATTN_ERR_DEVICE = 7           /* no usable sm_103 (B300) device */
 } bsattn_status;
 
 /* flags */
