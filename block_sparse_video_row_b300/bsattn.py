@@ -28,12 +28,15 @@ BSATTN_ERR_CUDA = 4
 BSATTN_ERR_OOM = 5
 BSATTN_ERR_TIMEOUT = 6
 BSATTN_ERR_DEVICE = 7
+BSATTN_ERR_INDEX = 8
 
 BSATTN_BOUND = 0
 BSATTN_ONLINE_MAX = 1
 BSATTN_NO_FALLBACK = 2
 BSATTN_BOUND_ONLY = 4
 BSATTN_DEBUG_STALL = 0x100
+BSATTN_DEBUG_CHECKS = 0x200
+BSATTN_DEBUG_PLANT_INDEX = 0x400
 BSATTN_ELIGIBLE_BOUND = 64.0
 BSATTN_PLAN_ONLY = 0x10
 

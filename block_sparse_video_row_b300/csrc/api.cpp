@@ -346,8 +346,10 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
                              bsattn_stream_t stream) {
     bsattn_status st = check_runnable(lay);
     if (st != BSATTN_OK) return st;
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_DEBUG_STALL)) != 0)
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_DEBUG_STALL |
+                   BSATTN_DEBUG_CHECKS | BSATTN_DEBUG_PLANT_INDEX)) != 0)
         return BSATTN_ERR_INVALID_ARG;
+    if ((flags & BSATTN_DEBUG_PLANT_INDEX) && !(flags & BSATTN_DEBUG_CHECKS)) return BSATTN_ERR_INVALID_ARG;
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BSATTN_ERR_INVALID_ARG;
@@ -368,6 +370,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.n_units = lay->n_slots;
     p.tile_ptr = lay->d_tile_ptr;
     p.tiles = lay->d_tiles;
+    p.n_tiles = static_cast<int32_t>(lay->tiles.size() / 2);
+    p.bh = lay->B * lay->H;
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
@@ -379,6 +383,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
     p.debug_stall = (flags & BSATTN_DEBUG_STALL) ? 1 : 0;
+    p.checks = (flags & BSATTN_DEBUG_CHECKS) ? 1 : 0;
+    p.debug_plant = (flags & BSATTN_DEBUG_PLANT_INDEX) ? 1 : 0;
     p.timeout_ns = lay->timeout_ns;
     const int grid = lay->grid;  // the width the schedule was built for
     auto launch = [&](bool on) {
@@ -395,6 +401,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     if (flags & BSATTN_NO_FALLBACK) return BSATTN_OK;
     p.mode = bsv::kModeFallback;
     p.debug_stall = 0;
+    p.debug_plant = 0;
     return from_cuda(launch(true));
 }
 
@@ -422,6 +429,7 @@ const char *bsattn_status_string(bsattn_status st) {
         case BSATTN_ERR_OOM: return "out of device memory";
         case BSATTN_ERR_TIMEOUT: return "a bounded device wait ran out";
         case BSATTN_ERR_DEVICE: return "no usable sm_103 device";
+        case BSATTN_ERR_INDEX: return "the device checks found a work unit or key tile out of range";
     }
     return "unknown status";
 }
@@ -437,7 +445,10 @@ bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, in
     if (e != cudaSuccess) return from_cuda(e);
     if (fallback_units) *fallback_units = h[4];
     if (fallback_rows) *fallback_rows = h[5];
-    if (device_status) *device_status = (h[0] & bsv::kStatusTimeout) ? BSATTN_ERR_TIMEOUT : BSATTN_OK;
+    if (device_status)
+        *device_status = (h[0] & bsv::kStatusTimeout) ? BSATTN_ERR_TIMEOUT
+                         : (h[0] & bsv::kStatusIndex) ? BSATTN_ERR_INDEX
+                                                       : BSATTN_OK;
     return BSATTN_OK;
 }
 

@@ -121,6 +121,53 @@ __device__ __forceinline__ int unit_index(const AttnParams &p, int i) {
     return p.mode == kModeFallback ? p.ws.fb_list[i] : i;
 }
 
+// The work unit of slot i, checked (device checks on): false when the slot, the unit
+// (head, query block, each query tile starting inside the frame), its key-tile range
+// or any key tile it reads (16-aligned start, width 16..kKvTile, inside the head's
+// L_kv keys) is out of range.  Reads only what the checks before it allowed.
+__device__ __forceinline__ bool fetch_unit_checked(const AttnParams &p, int i, int &u, int4 &U, bool report) {
+    bool ok = i >= 0 && i < p.n_units;
+    if (ok) {
+        u = unit_index(p, i);
+        ok = u >= 0 && u < p.n_units;
+    }
+    if (ok) {
+        U = p.units[u];
+        ok = U.w >= 0 && U.w <= 2;
+        if (ok && U.w > 0) {
+            ok = U.x >= 0 && U.x < p.bh && U.y >= 0 && U.y < p.nb && U.z >= 0 &&
+                 (static_cast<int64_t>(U.z) + U.w - 1) * kQTile < p.block;
+            if (ok) {
+                const int a = p.tile_ptr[U.y], b = p.tile_ptr[U.y + 1];
+                ok = a >= 0 && a <= b && b <= p.n_tiles;
+                for (int t = a; ok && t < b; ++t) {
+                    int2 T = p.tiles[t];
+                    // testing only: the CTA's first unit sees its first key tile past the last key
+                    if (p.debug_plant && t == a && i == static_cast<int>(blockIdx.x)) T.x = static_cast<int>(p.Lkv);
+                    ok = T.x >= 0 && (T.x & 15) == 0 && T.y >= 16 && T.y <= kKvTile && (T.y & 15) == 0 &&
+                         static_cast<int64_t>(T.x) + T.y <= p.Lkv;
+                }
+            }
+        }
+    }
+    if (!ok) {
+        u = 0;
+        U = make_int4(0, 0, 0, 0);
+        if (report) atomicOr(p.ws.status, kStatusIndex);
+    }
+    return ok;
+}
+
+// The work unit of slot i.  With device checks on, false for a unit the checks
+// reject; the caller skips it.  Every role calls this with the same i, so all roles
+// skip the same units; only the caller with `report` records the status bit.
+__device__ __forceinline__ bool fetch_unit(const AttnParams &p, int i, int &u, int4 &U, bool report) {
+    if (p.checks) return fetch_unit_checked(p, i, u, U, report);
+    u = unit_index(p, i);
+    U = p.units[u];
+    return true;
+}
+
 // Wait that ignores the abort flag: used only to let already-issued copies/MMAs land.
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
     const uint32_t a = smem_u32(bar);
@@ -340,7 +387,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             uint32_t gk = 0, gv = 0;  // K / V copies issued
             bool ok = true;
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
-                const int4 U = p.units[unit_index(p, i)];
+                int u;
+                int4 U;
+                if (!fetch_unit(p, i, u, U, true)) continue;  // rejected by the device checks
                 const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
                 if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
                 // testing only: the first unit's query tiles are never loaded, so the
@@ -425,7 +474,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             uint32_t g = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
-                const int4 U = p.units[unit_index(p, i)];
+                int u;
+                int4 U;
+                if (!fetch_unit(p, i, u, U, false)) continue;  // rejected by the device checks
                 const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
                 if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
                 if (t >= U.w) {
@@ -517,8 +568,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t s_uses0 = 0, s_uses1 = 0, o_uses0 = 0, o_uses1 = 0, x_uses = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
-            const int u = unit_index(p, i);
-            const int4 U = p.units[u];
+            int u;
+            int4 U;
+            if (!fetch_unit(p, i, u, U, false)) continue;  // rejected by the device checks
             const int nt = U.w;
             if (nt == 0) continue;  // an empty schedule slot
             const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;

@@ -125,7 +125,8 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != lay->device) return BSATTN_ERR_INVALID_ARG;
     if (!q || !k || !v || !o || pairs_per_chunk < 0) return BSATTN_ERR_INVALID_ARG;
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY)) != 0) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_DEBUG_CHECKS)) != 0)
+        return BSATTN_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
     const int32_t BH = lay->B * lay->H;
     // About eight chunks: enough to overlap copies with kernels, each still a full grid.

@@ -17,13 +17,14 @@ constexpr int kRegsLow = 72;          // TMA / MMA warpgroup after setmaxnreg.de
 constexpr int kRegsHigh = 208;        // softmax warpgroups after setmaxnreg.inc
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kAttnThreads * kLaunchRegs, "register split");
 constexpr float kGuardTau = 5.421010862427522e-20f;  // 2^-64: smallest denominator trusted
-constexpr int kStatusTimeout = 1;     // bit in the device status word
+constexpr int kStatusTimeout = 1;     // bits in the device status word: a bounded wait ran out,
+constexpr int kStatusIndex = 2;       // the device checks rejected a work unit
 
 // Device-side workspace of a layout (one allocation, zeroed per forward where noted).
 struct Workspace {
     int32_t *fb_count;   // units appended to the fallback list      (zeroed per forward)
     int32_t *fb_rows;    // rows flagged by the guard                  (zeroed per forward)
-    int32_t *status;     // device status bits (kStatusTimeout)        (zeroed at create)
+    int32_t *status;     // device status bits (kStatus*)              (zeroed at create)
     int32_t *unit_flag;  // per work unit: flagged already             (zeroed per forward)
     int32_t *fb_list;    // work-unit indices to rerun
 };
@@ -39,6 +40,8 @@ struct AttnParams {
     int32_t n_units;
     const int32_t *tile_ptr;  // key tiles of query block qb: tiles[tile_ptr[qb] .. tile_ptr[qb+1])
     const int2 *tiles;        // (first key within the head, width: a multiple of 16, <= kKvTile)
+    int32_t n_tiles;          // entries of tiles
+    int32_t bh;               // B * H
     const float *rowbound;    // [B*H*L]
     uint16_t *o;              // [B*H*L, D] bf16 bits
     float *lse;               // [B*H*L] or null
@@ -51,6 +54,8 @@ struct AttnParams {
     float elig_m;             // rows with a larger bound use the online max (kModeBound only)
     int32_t mode;
     int32_t debug_stall;      // testing: skip the first unit's query-tile loads (waits run out)
+    int32_t checks;           // device-side index checks of every unit before use
+    int32_t debug_plant;      // testing, with checks: the first unit's first key tile reads as out of range
     uint64_t timeout_ns;
 };
 

@@ -81,6 +81,12 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     if ((reinterpret_cast<uintptr_t>(rowbound) & 3) || (reinterpret_cast<uintptr_t>(lse) & 3))
         return BSATTN_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+    // The plan is copied from a host buffer that lives only during this call, so a
+    // graph captured from it would read freed memory at replay.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &capture) != cudaSuccess)
+        return BSATTN_ERR_CUDA;
+    if (capture != cudaStreamCaptureStatusNone) return BSATTN_ERR_UNSUPPORTED;
 
     // The work plan, built on the host only (the plan-only layout touches no device).
     bsattn_layout_t plan = nullptr;
@@ -141,6 +147,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.n_units = info.n_units;
     p.tile_ptr = reinterpret_cast<const int32_t *>(base + off_tileptr);
     p.tiles = reinterpret_cast<const int2 *>(base + off_tiles);
+    p.n_tiles = info.key_tiles;
+    p.bh = info.B * info.H;
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
@@ -156,6 +164,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
     p.debug_stall = 0;
+    p.checks = 0;
+    p.debug_plant = 0;
     uint64_t ms = 4000;
     if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
         const long long val = std::atoll(env);

@@ -74,7 +74,8 @@ typedef enum {
     BSATTN_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
     BSATTN_ERR_OOM = 5,             /* device allocation failed at create */
     BSATTN_ERR_TIMEOUT = 6,         /* a bounded device wait ran out (reported by query_stats) */
-    BSATTN_ERR_DEVICE = 7           /* no usable sm_103 (B300) device */
+    BSATTN_ERR_DEVICE = 7,          /* no usable sm_103 (B300) device */
+    BSATTN_ERR_INDEX = 8            /* device checks found a work unit or key tile out of range */
 } bsattn_status;
 
 /* flags */
@@ -100,6 +101,19 @@ enum {
        returns, bsattn_query_stats reports BSATTN_ERR_TIMEOUT and o is undefined.
        The GPU context stays usable. */
     BSATTN_DEBUG_STALL = 0x100,
+    /* bsattn_forward (and bsattn_forward_host): device-side index checks.  Before
+       any role of the kernel uses a work unit, it checks the unit (head, query
+       block, query tiles against the frame) and every key tile the unit reads
+       (start and width against L_kv, 16-aligned, width 16..128) against the
+       layout's tables.  A unit that fails is skipped by every role (its rows of o
+       and lse are left as they were), bit BSATTN_ERR_INDEX is recorded in the
+       layout's status word and bsattn_query_stats reports it.  Nothing traps.
+       Costs one pass over the unit's tile list per role; off by default. */
+    BSATTN_DEBUG_CHECKS = 0x200,
+    /* bsattn_forward, testing only, and only together with BSATTN_DEBUG_CHECKS:
+       the device checks see the first key tile of every CTA's first work unit as
+       starting at L_kv (past the last key), so they reject that unit. */
+    BSATTN_DEBUG_PLANT_INDEX = 0x400,
     /* bsattn_create_layout: build the host plan only, touch no device; such a
        layout can be inspected (info/export) but not run. */
     BSATTN_PLAN_ONLY = 0x10
@@ -179,7 +193,9 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
  *   rowbound  fp32 [B, H, L] from bsattn_row_bounds (unused with BSATTN_ONLINE_MAX; may be NULL then).
  *   lse       optional fp32 [B, H, L] out: the natural log of the softmax denominator,
  *             ln sum_j exp(scale * q_i . k_j) over allowed keys (-inf for rows that read nothing).
- *   flags     BSATTN_BOUND (0), BSATTN_ONLINE_MAX, BSATTN_NO_FALLBACK, BSATTN_BOUND_ONLY.
+ *   flags     BSATTN_BOUND (0), BSATTN_ONLINE_MAX, BSATTN_NO_FALLBACK, BSATTN_BOUND_ONLY,
+ *             BSATTN_DEBUG_CHECKS, and the testing flags BSATTN_DEBUG_STALL and
+ *             BSATTN_DEBUG_PLANT_INDEX (the latter only with BSATTN_DEBUG_CHECKS).
  * BSATTN_BOUND computes P = exp(scale * S - m_i) with no running max, rounds P
  * to bf16 for the P.V product and sums the denominator from the same rounded
  * values.  Each warp of the kernel owns 32 rows of a 128-row query tile; when
@@ -201,7 +217,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
  *   q, k, v   host bf16 [B, H, L, D] in; o host bf16 [B, H, L, D] out.  Page-locked
  *             (pinned) memory lets the copies run asynchronously and overlap the
  *             kernels; pageable memory works but the copies then serialise.
- *   scale, flags  as for bsattn_forward (BSATTN_ONLINE_MAX skips the row bounds).
+ *   scale, flags  as for bsattn_forward (BSATTN_ONLINE_MAX skips the row bounds;
+ *             the testing flags are refused).
  *   lse       optional host fp32 [B, H, L] out, as for bsattn_forward.
  *   pairs_per_chunk  (batch, head) pairs per pipeline chunk; 0 picks about eight
  *             chunks.
@@ -242,10 +259,11 @@ bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q, const void
  * work units (the 720p chunk uses 4,680, the 1080p chunk 9,984); a larger
  * problem returns BSATTN_ERR_UNSUPPORTED before any device work.
  * The first call on a device (with that device current) looks up the array's
- * device address; make that first call before any stream capture.  Each call
- * copies the plan and zeroed guard counters into the array with one
- * cudaMemcpyAsync from host memory on `stream`, so the call may wait for work
- * already queued on that stream.  All calls share the array and it keeps the
+ * device address.  Each call copies the plan and zeroed guard counters into the
+ * array with one cudaMemcpyAsync from a host buffer that lives only during the
+ * call, on `stream`, so the call may wait for work already queued on that stream,
+ * and it cannot be captured in a CUDA graph: on a capturing stream it returns
+ * BSATTN_ERR_UNSUPPORTED before any work (use a layout and bsattn_forward there).  All calls share the array and it keeps the
  * last call's contents: calls whose GPU work overlaps (other streams, other
  * host threads) race.  Statistics are not kept (bsattn_query_stats needs a layout).
  * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA or DEVICE.
@@ -268,8 +286,10 @@ const char *bsattn_status_string(bsattn_status st);
  * Statistics of the last bsattn_forward on this layout.  Synchronises `stream`.
  *   fallback_rows   rows flagged by the underflow guard (nullable).
  *   fallback_units  work units rerun with the online-max kernel (nullable).
- *   device_status   BSATTN_OK, or BSATTN_ERR_TIMEOUT if a bounded device wait
- *                   ran out since the layout was created (nullable).
+ *   device_status   BSATTN_OK; BSATTN_ERR_TIMEOUT if a bounded device wait ran
+ *                   out since the layout was created; else BSATTN_ERR_INDEX if
+ *                   the device checks (BSATTN_DEBUG_CHECKS) rejected a work unit
+ *                   since then (nullable).
  */
 bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, int64_t *fallback_units,
                                  int32_t *device_status, bsattn_stream_t stream);

@@ -357,6 +357,55 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable(ba, monkeypatch):
     full_case(ba, q, k, v, mask, w.block, w.scale, what="after a timeout")
 
 
+def _mid_case():
+    # 192 work units (8 heads x 6 frames x 4 pairs of query tiles): more than one per CTA
+    B, H, nf, bs, D = 1, 8, 6, 1024, 128
+    L = nf * bs
+    q = synth.tensor_bf16(31, synth.TAG_Q, B, H, L, D)
+    k = synth.tensor_bf16(31, synth.TAG_K, B, H, L, D)
+    v = synth.tensor_bf16(31, synth.TAG_V, B, H, L, D)
+    return q, k, v, synth.window_mask(nf, 1), bs, 1.0 / np.sqrt(D)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "stream_small", "mid"])
+def test_device_checks_accept_valid_plans_and_change_nothing(ba, name):
+    # BSATTN_DEBUG_CHECKS on a valid plan: no unit rejected (status stays ok) and the
+    # output is bit-identical to the unchecked launch.
+    if name == "mid":
+        q, k, v, mask, bs, scale = _mid_case()
+    else:
+        w = synth.WORKLOADS[name]
+        q, k, v = synth.make_qkv(w)
+        mask, bs, scale = w.block_mask(), w.block, w.scale
+    plain = run_gpu(ba, q, k, v, mask, bs, scale, 0, want_meta=False)
+    checked = run_gpu(ba, q, k, v, mask, bs, scale, ba.BSATTN_DEBUG_CHECKS, want_meta=False)
+    assert plain["status"] == 0 and checked["status"] == 0
+    assert torch.equal(plain["o_raw"].view(torch.int16), checked["o_raw"].view(torch.int16))
+
+
+def test_device_checks_reject_a_planted_key_tile(ba):
+    # Testing flag: the checks see the first key tile of every CTA's first work unit as
+    # starting past the last key.  Every role skips those units (their rows keep the NaN
+    # the output was filled with, whole query tiles at a time), the other units match the
+    # oracle, no rerun touches the skipped ones, and the layout reports the index status.
+    q, k, v, mask, bs, scale = _mid_case()
+    B, H, L, D = q.shape
+    res = run_gpu(ba, q, k, v, mask, bs, scale, ba.BSATTN_DEBUG_CHECKS | ba.BSATTN_DEBUG_PLANT_INDEX,
+                  want_meta=False)
+    assert res["status"] == ba.BSATTN_ERR_INDEX
+    assert res["fb_rows"] == 0
+    skipped = np.isnan(res["o"]).all(axis=1)
+    assert np.array_equal(skipped, np.isnan(res["o"]).any(axis=1))
+    tiles = skipped.reshape(B * H, L // bs, bs // 128, 128)
+    assert np.all(tiles.all(axis=3) == tiles.any(axis=3)), "a query tile was skipped in part"
+    n_tiles_skipped = int(tiles.all(axis=3).sum())
+    grid = min(B * H * (L // bs) * (bs // 256), torch.cuda.get_device_properties(0).multi_processor_count)
+    assert 0 < n_tiles_skipped <= 2 * grid
+    assert n_tiles_skipped < tiles.shape[0] * tiles.shape[1] * tiles.shape[2]
+    O, _, _ = oracle.attention(q, k, v, mask, bs, scale)
+    check_o(res["o"][~skipped], O[~skipped], "units the checks let through")
+
+
 def test_cuda_graph_capture_and_replay(ba):
     # A whole step (row bounds + forward with its memset, bound kernel and rerun launch)
     # captured once in a CUDA graph and replayed on new inputs copied into the same buffers:

@@ -148,7 +148,7 @@ def test_plan_only_layout_refuses_device_calls(lib):
 
 
 def test_status_strings(lib):
-    for st in range(8):
+    for st in range(9):
         assert isinstance(bsattn.status_string(st), str) and bsattn.status_string(st)
     assert bsattn.status_string(99) == "unknown status"
 

@@ -91,3 +91,20 @@ def test_noalloc_rejects_plans_beyond_its_array(ba):
     st = ba.bsattn_forward_noalloc(fake, fake, fake, fake, 1, 512, 13 * 3600, 128, 3600, mask, 0.088, fake, None,
                                    0, raise_on_error=False)
     assert st == ba.BSATTN_ERR_UNSUPPORTED
+
+
+def test_noalloc_refuses_stream_capture(ba):
+    # Its plan copy reads a host buffer that is gone once the call returns, so a captured
+    # graph would replay a copy from freed memory: the call refuses a capturing stream
+    # before any work (nothing is captured).
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = synth.make_qkv(w)
+    dq, dk, dv = _dev(q), _dev(k), _dev(v)
+    o = torch.empty_like(dq)
+    rb = torch.ones((w.B, w.H, w.L), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = ba.bsattn_forward_noalloc(dq, dk, dv, o, w.B, w.H, w.L, w.D, w.block, w.block_mask(), w.scale, rb,
+                                       None, 0, raise_on_error=False)
+    assert st == ba.BSATTN_ERR_UNSUPPORTED
