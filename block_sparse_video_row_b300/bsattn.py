@@ -114,6 +114,55 @@ def _ptr(x) -> Optional[int]:
     raise TypeError(f"cannot pass {type(x)} as a pointer")
 
 
+def _check_arg(name: str, x, numel: int, itemsize: int, on_device: bool) -> None:
+    """A torch tensor or numpy array given for a C-ABI pointer must be contiguous and hold
+    exactly `numel` elements of `itemsize` bytes on the side the call reads it from (the
+    current CUDA device, or host memory): the library sees only the pointer, so a wrong
+    size or a host pointer in a kernel would read out of bounds.  Integer pointers and
+    None pass unchecked."""
+    if x is None or isinstance(x, int):
+        return
+    if hasattr(x, "data_ptr"):  # torch.Tensor
+        if not x.is_contiguous():
+            raise ValueError(f"{name}: tensor must be contiguous")
+        import torch
+        ok = x.dtype == torch.float32 if itemsize == 4 else x.dtype in (torch.bfloat16, torch.int16, torch.uint16)
+        if not ok:
+            raise TypeError(f"{name}: expected {'bf16 (or its 16-bit pattern)' if itemsize == 2 else 'fp32'} "
+                            f"elements, got {x.dtype}")
+        if x.numel() != numel:
+            raise ValueError(f"{name}: {x.numel()} elements, expected {numel}")
+        if on_device:
+            if not x.is_cuda or x.device.index != torch.cuda.current_device():
+                raise TypeError(f"{name}: must be a tensor on the current CUDA device (got {x.device})")
+        elif x.is_cuda:
+            raise TypeError(f"{name}: must be a host tensor")
+        return
+    if isinstance(x, np.ndarray):
+        if on_device:
+            raise TypeError(f"{name}: a numpy array is host memory; this call takes device pointers")
+        if not x.flags.c_contiguous:
+            raise ValueError(f"{name}: array must be C-contiguous")
+        if x.itemsize != itemsize or (itemsize == 4 and x.dtype.kind != "f"):
+            raise TypeError(f"{name}: expected {'bf16 bits (2-byte)' if itemsize == 2 else 'float32'} elements")
+        if x.size != numel:
+            raise ValueError(f"{name}: {x.size} elements, expected {numel}")
+        return
+    raise TypeError(f"{name}: cannot pass {type(x)} as a pointer")
+
+
+def _check_io(lay: "Layout", on_device: bool, q=None, k=None, v=None, o=None, rows=(), kmax=None) -> None:
+    i = lay.info
+    BH = i.B * i.H
+    for name, x in (("q", q), ("o", o)):
+        _check_arg(name, x, BH * i.L * i.D, 2, on_device)
+    for name, x in (("k", k), ("v", v)):
+        _check_arg(name, x, BH * i.L_kv * i.D, 2, on_device)
+    for name, x in rows:
+        _check_arg(name, x, BH * i.L, 4, on_device)
+    _check_arg("kmax", kmax, BH * i.nb_kv, 4, on_device)
+
+
 def _stream(s) -> Optional[int]:
     if s is None:
         try:
@@ -190,6 +239,8 @@ def bsattn_create_layout_rect(B: int, H: int, L: int, L_kv: int, D: int, block_s
 
 def bsattn_row_bounds(lay: Layout, q, k, scale: float, qnorm, kmax, rowbound, stream=None,
                       raise_on_error: bool = True) -> int:
+    if lay.handle:
+        _check_io(lay, True, q=q, k=k, rows=(("qnorm", qnorm), ("rowbound", rowbound)), kmax=kmax)
     st = load().bsattn_row_bounds(lay.handle, _ptr(q), _ptr(k), float(scale), _ptr(qnorm), _ptr(kmax),
                                   _ptr(rowbound), _stream(stream))
     if raise_on_error:
@@ -199,6 +250,8 @@ def bsattn_row_bounds(lay: Layout, q, k, scale: float, qnorm, kmax, rowbound, st
 
 def bsattn_forward(lay: Layout, q, k, v, o, scale: float, rowbound, lse=None, flags: int = 0, stream=None,
                    raise_on_error: bool = True) -> int:
+    if lay.handle:
+        _check_io(lay, True, q=q, k=k, v=v, o=o, rows=(("rowbound", rowbound), ("lse", lse)))
     st = load().bsattn_forward(lay.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), float(scale), _ptr(rowbound),
                                _ptr(lse), flags, _stream(stream))
     if raise_on_error:
@@ -212,6 +265,11 @@ def bsattn_forward_noalloc(q, k, v, o, B: int, H: int, L: int, D: int, block_siz
     """The forward without a layout, for callers that may not allocate device memory
     (see bsattn_forward_noalloc in include/bsattn.h)."""
     m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
+    n = B * H * L
+    for name, x in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_arg(name, x, n * D, 2, True)
+    for name, x in (("rowbound", rowbound), ("lse", lse)):
+        _check_arg(name, x, n, 4, True)
     st = load().bsattn_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, L, D, block_size, m.ctypes.data,
                                        float(scale), _ptr(rowbound), _ptr(lse), flags, _stream(stream))
     if raise_on_error:
@@ -224,9 +282,7 @@ def bsattn_forward_host(lay: Layout, q, k, v, o, scale: float, lse=None, flags: 
     """Row bounds + forward for host tensors (pinned CPU torch tensors or numpy arrays): copies,
     kernels and copy-out pipelined per chunk of (batch, head) pairs; synchronise `stream` before
     reading o."""
-    for x in (q, k, v, o) + ((lse,) if lse is not None else ()):
-        if hasattr(x, "is_cuda") and x.is_cuda:
-            raise TypeError("bsattn_forward_host takes host tensors")
+    _check_io(lay, False, q=q, k=k, v=v, o=o, rows=(("lse", lse),))
     _check(load().bsattn_forward_host(lay.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), float(scale), _ptr(lse),
                                       flags, pairs_per_chunk, _stream(stream)), "bsattn_forward_host")
 

@@ -159,3 +159,30 @@ def test_device_layout_without_gpu_reports_an_error(lib):
         pytest.skip("a GPU is present")
     st, lay = bsattn.bsattn_create_layout(1, 2, 192, 64, 48, synth.window_mask(4, 1), 0, raise_on_error=False)
     assert st in (bsattn.BSATTN_ERR_DEVICE, bsattn.BSATTN_ERR_CUDA) and lay is None
+
+
+def test_binding_checks_tensor_arguments(lib):
+    # The C ABI sees only pointers, so the binding checks torch / numpy arguments first:
+    # a host tensor where device memory is read, a wrong element type, a strided view or
+    # a wrong element count is refused before any call into the library.
+    import torch
+    lay = bsattn.bsattn_create_layout(1, 2, 192, 64, 48, synth.window_mask(4, 1), bsattn.BSATTN_PLAN_ONLY)
+    q = torch.zeros(1, 2, 192, 64, dtype=torch.bfloat16)
+    rb = torch.zeros(1, 2, 192)
+    with pytest.raises(TypeError, match="CUDA device"):
+        bsattn.bsattn_forward(lay, q, q, q, q, 0.125, rb)
+    with pytest.raises(TypeError, match="bf16"):
+        bsattn.bsattn_forward(lay, q.float(), q, q, q, 0.125, rb)
+    with pytest.raises(ValueError, match="contiguous"):
+        bsattn.bsattn_forward(lay, q.transpose(2, 3), q, q, q, 0.125, rb)
+    with pytest.raises(TypeError, match="fp32"):
+        bsattn.bsattn_row_bounds(lay, 1 << 20, 1 << 20, 0.125, rb.double(), 1 << 20, 1 << 20)
+    with pytest.raises(ValueError, match="elements"):
+        bsattn.bsattn_forward_host(lay, q, q, q, q[:, :1], 0.125)
+    with pytest.raises(TypeError, match="host"):
+        bsattn.bsattn_forward_noalloc(np.zeros(q.shape, np.uint16), 1 << 20, 1 << 20, 1 << 20, 1, 2, 192, 64, 48,
+                                      synth.window_mask(4, 1), 0.125, 1 << 20)
+    # right sizes on the host pass the binding; the library then refuses the plan-only layout
+    with pytest.raises(bsattn.BsattnError):
+        bsattn.bsattn_forward_host(lay, q, q, q, torch.empty_like(q), 0.125)
+    lay.destroy()
