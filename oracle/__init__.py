@@ -14,7 +14,8 @@ explicit -inf mask, torch's fp64 scaled_dot_product_attention on an all-ones
 mask, closed forms (q = 0, equal keys, constant values, one dominant key,
 permutation inside a block, two-key softmax), the Cauchy-Schwarz invariant,
 shift invariance of the softmax (bound shift vs max shift), and the fp32 norm
-recipe against fp64 norms and exact special cases.
+recipe against fp64 norms and exact special cases.  Per-head masks ([H, nbq,
+nbkv]) are the same routines run head by head, pinned by brute force per head.
 """
 from __future__ import annotations
 
@@ -99,6 +100,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, blo
     rows: global query row ids into B*H*Lq (None = all).
     Returns (O [nrows, D] fp64, LSE [nrows], l [nrows]) where l = sum_j exp(S_ij - shift_i)
     (shift = row max when ``shift`` is None)."""
+    if np.ndim(mask) == 3:
+        return _attention_per_head(q, k, v, np.asarray(mask), block, scale, rows, shift, nthreads)
     q, k, v = _u16(q), _u16(k), _u16(v)
     B, H, Lq, D = q.shape
     Lkv = k.shape[2]
@@ -119,6 +122,28 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, blo
     return out, lse, lsum
 
 
+def _attention_per_head(q, k, v, mask, block, scale, rows, shift, nthreads):
+    """One mask per head (mask [H, nbq, nbkv]): the heads are independent attentions, so
+    head h is the plain masked attention of its own slice of Q, K, V under mask[h]."""
+    B, H, Lq, D = q.shape
+    assert mask.shape[0] == H
+    grow = np.arange(B * H * Lq, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    bh, i = grow // Lq, grow % Lq
+    b, h = bh // H, bh % H
+    out = np.empty((len(grow), D), dtype=np.float64)
+    lse = np.empty(len(grow), dtype=np.float64)
+    lsum = np.empty(len(grow), dtype=np.float64)
+    for hh in range(H):
+        sel = np.nonzero(h == hh)[0]
+        if len(sel) == 0:
+            continue
+        o_h, lse_h, l_h = attention(q[:, hh:hh + 1], k[:, hh:hh + 1], v[:, hh:hh + 1], mask[hh], block, scale,
+                                    rows=b[sel] * Lq + i[sel], shift=None if shift is None else shift[sel],
+                                    nthreads=nthreads)
+        out[sel], lse[sel], lsum[sel] = o_h, lse_h, l_h
+    return out, lse, lsum
+
+
 def row_norms_f64(x: np.ndarray) -> np.ndarray:
     x = _u16(x)
     D = x.shape[-1]
@@ -128,7 +153,11 @@ def row_norms_f64(x: np.ndarray) -> np.ndarray:
 
 
 def row_bounds_f64(qnorm: np.ndarray, knorm: np.ndarray, mask: np.ndarray, block: int, scale: float):
-    """M_i = scale * |q_i| * max_{j allowed} |k_j| in fp64; qnorm [B,H,Lq], knorm [B,H,Lkv]."""
+    """M_i = scale * |q_i| * max_{j allowed} |k_j| in fp64; qnorm [B,H,Lq], knorm [B,H,Lkv]
+    (mask [H, nbq, nbkv]: head h under mask[h])."""
+    if np.ndim(mask) == 3:
+        return np.concatenate([row_bounds_f64(qnorm[:, h:h + 1], knorm[:, h:h + 1], mask[h], block, scale)
+                               for h in range(np.shape(qnorm)[1])], axis=1)
     qn = np.ascontiguousarray(qnorm, dtype=np.float64)
     kn = np.ascontiguousarray(knorm, dtype=np.float64)
     B, H, Lq = qn.shape
@@ -158,6 +187,10 @@ def block_max_f32(knorm: np.ndarray, block: int) -> np.ndarray:
 
 
 def row_bounds_f32(qnorm: np.ndarray, kmax: np.ndarray, mask: np.ndarray, block: int, scale: float):
+    """fl(fl(scale * qnorm_i) * max over the allowed key blocks of kmax) (mask [H, nbq, nbkv]: head h under mask[h])."""
+    if np.ndim(mask) == 3:
+        return np.concatenate([row_bounds_f32(qnorm[:, h:h + 1], kmax[:, h:h + 1], mask[h], block, scale)
+                               for h in range(np.shape(qnorm)[1])], axis=1)
     qn = np.ascontiguousarray(qnorm, dtype=np.float32)
     km = np.ascontiguousarray(kmax, dtype=np.float32)
     B, H, Lq = qn.shape

@@ -370,3 +370,80 @@ def test_generator_matches_splitmix64_definition():
     assert list(synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(x))) == [1.0, 1 + 2 ** -6, 1 + 2 ** -7]
     q = _f64(synth.tensor_bf16(0, synth.TAG_Q, 1, 2, 4096, 64))
     assert abs(q.mean()) < 0.01 and abs(q.std() - 1) < 0.01
+
+
+# ------------------------------------------------------------------------------------------------
+# one block mask per head
+
+
+def _per_head_masks(nb, rng):
+    m0 = synth.window_mask(nb, 1)
+    m1 = (rng.random((nb, nb)) < 0.5).astype(np.uint8)
+    m1[1, :] = 0  # a query block that reads nothing under this head's mask
+    m2 = np.ones((nb, nb), np.uint8)
+    return np.stack([m0, m1, m2])
+
+
+def test_per_head_masks_brute_force():
+    # Each head under its own mask: the dense route builds head h's element mask from
+    # mask[h] (numpy, independent of the oracle's slicing); all rows and sampled rows.
+    rng = np.random.default_rng(5)
+    B, H, D, nb, bs = 2, 3, 64, 5, 16
+    L = nb * bs
+    masks = _per_head_masks(nb, rng)
+    q, k, v = _rand_qkv(B, H, L, D, seed=13)
+    scale = 0.125
+    O, lse, _ = oracle.attention(q, k, v, masks, bs, scale)
+    Ob = np.zeros((B, H, L, D))
+    lseb = np.zeros((B, H, L))
+    for h in range(H):
+        o_h, l_h = _brute_dense(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], masks[h], bs, scale)
+        Ob[:, h] = o_h.reshape(B, L, D)
+        lseb[:, h] = l_h.reshape(B, L)
+    Ob, lseb = Ob.reshape(-1, D), lseb.reshape(-1)
+    assert np.max(np.abs(O - Ob)) <= 1e-12
+    fin = np.isfinite(lseb)
+    assert np.array_equal(fin, np.isfinite(lse)) and np.max(np.abs(lse[fin] - lseb[fin])) <= 1e-12
+    # head 1's empty query block: O = 0 there, other heads' rows of that block are not empty
+    rows = np.arange(B * H * L)
+    empty = ((rows // L) % H == 1) & ((rows % L) // bs == 1)
+    assert np.all(O[empty] == 0) and np.all(np.isneginf(lse[empty]))
+    assert np.all(np.isfinite(lse[~empty]))
+    # the sampled-row route gives the same rows
+    pick = rng.choice(B * H * L, 37, replace=False)
+    Os, lses, _ = oracle.attention(q, k, v, masks, bs, scale, rows=pick)
+    assert np.array_equal(Os, O[pick]) and np.array_equal(lses, lse[pick])
+
+
+def test_per_head_masks_equal_masks_match_the_shared_mask():
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = synth.make_qkv(w)
+    m = w.block_mask()
+    O1, lse1, l1 = oracle.attention(q, k, v, m, w.block, w.scale)
+    O2, lse2, l2 = oracle.attention(q, k, v, np.stack([m] * w.H), w.block, w.scale)
+    assert np.array_equal(O1, O2) and np.array_equal(lse1, lse2) and np.array_equal(l1, l2)
+    _, _, rb1 = oracle.metadata_f32(q, k, m, w.block, w.scale)
+    _, _, rb2 = oracle.metadata_f32(q, k, np.stack([m] * w.H), w.block, w.scale)
+    assert np.array_equal(rb1.view(np.uint32), rb2.view(np.uint32))
+
+
+def test_per_head_row_bounds_by_hand():
+    # M_i = scale * |q_i| * max over head h's allowed key blocks of |k_j|, computed here with
+    # numpy from the definition; every allowed logit of the head lies below it.
+    rng = np.random.default_rng(9)
+    B, H, D, nb, bs = 1, 3, 64, 5, 16
+    L = nb * bs
+    masks = _per_head_masks(nb, rng)
+    q, k, _ = _rand_qkv(B, H, L, D, seed=17)
+    qf, kf = _f64(q), _f64(k)
+    qn, kn = np.sqrt((qf ** 2).sum(-1)), np.sqrt((kf ** 2).sum(-1))
+    M = oracle.row_bounds_f64(qn, kn, masks, bs, 0.125)
+    for h in range(H):
+        kblk = kn[0, h].reshape(nb, bs).max(axis=1)
+        for i in range(L):
+            allowed = np.nonzero(masks[h, i // bs])[0]
+            want = 0.125 * qn[0, h, i] * (kblk[allowed].max() if len(allowed) else 0.0)
+            assert M[0, h, i] == pytest.approx(want, rel=1e-15, abs=0.0)
+            if len(allowed):
+                keys = np.concatenate([np.arange(kb * bs, kb * bs + bs) for kb in allowed])
+                assert np.all(0.125 * (kf[0, h, keys] @ qf[0, h, i]) <= M[0, h, i] * (1 + 1e-12))
