@@ -125,7 +125,8 @@ def cpu_oracle_sample(q, k, v, w, seconds: float, seed: int = 1):
     import oracle
     rng = np.random.default_rng(seed)
     mask = w.block_mask()
-    allowed_keys = mask.sum(axis=1) * w.block  # per query frame
+    # allowed keys per (mask, query frame): one mask for all heads, or one per head
+    allowed_keys = (mask if mask.ndim == 3 else mask[None]).sum(axis=2) * w.block
     n_total = w.B * w.H * w.L
 
     def run(nrows):
@@ -134,7 +135,8 @@ def cpu_oracle_sample(q, k, v, w, seconds: float, seed: int = 1):
         oracle.attention(q, k, v, mask, w.block, w.scale, rows=rows)
         dt = time.perf_counter() - t0
         frames = (rows % w.L) // w.block
-        flop = float(np.sum(4.0 * allowed_keys[frames] * w.D))
+        heads = (rows // w.L) % w.H if mask.ndim == 3 else np.zeros_like(rows)
+        flop = float(np.sum(4.0 * allowed_keys[heads, frames] * w.D))
         return flop, dt
 
     cores = oracle.n_threads()
@@ -169,7 +171,8 @@ def main():
     flop_step = synth.useful_flop(w)
     config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "L_kv": w.L_kv, "D": w.D, "frames": w.frames,
               "query_frames": w.nq,
-              "block": w.block, "mask": "frame window" + (" + first frame" if w.block_mask()[-1, 0] else ""),
+              "block": w.block, "mask": ("one per head (four rules cycling)" if w.block_mask().ndim == 3 else
+                                          "frame window" + (" + first frame" if w.block_mask()[-1, 0] else "")),
               "nnz_blocks": int(w.block_mask().sum()), "keys": w.keys, "seed": w.seed,
               "useful_flop_per_step": flop_step,
               "l2": "inputs larger than L2 (Q+K+V+O %.2f GB > 126 MB), no flush"

@@ -39,6 +39,7 @@ BSATTN_DEBUG_CHECKS = 0x200
 BSATTN_DEBUG_PLANT_INDEX = 0x400
 BSATTN_ELIGIBLE_BOUND = 64.0
 BSATTN_PLAN_ONLY = 0x10
+BSATTN_MASK_PER_HEAD = 0x20
 
 EXPORTED = ("bsattn_create_layout", "bsattn_create_layout_rect", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
             "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export",
@@ -51,7 +52,7 @@ class LayoutInfo(ctypes.Structure):
                 ("nnz_blocks", ctypes.c_int32), ("kv_tile", ctypes.c_int32), ("key_tiles", ctypes.c_int32),
                 ("q_tiles_per_block", ctypes.c_int32), ("n_units", ctypes.c_int32),
                 ("mma_rows", ctypes.c_int64), ("useful_flop", ctypes.c_double), ("L_kv", ctypes.c_int64),
-                ("nb_kv", ctypes.c_int32)]
+                ("nb_kv", ctypes.c_int32), ("mask_heads", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -216,8 +217,13 @@ def bsattn_create_layout(B: int, H: int, L: int, D: int, block_size: int, block_
                          raise_on_error: bool = True, L_kv: Optional[int] = None):
     """Returns a Layout (or, with raise_on_error=False, the pair (status, Layout or None)).
     L_kv (key tokens, default L) other than L builds a streamed-chunk layout through
-    bsattn_create_layout_rect; block_mask is then [L / block_size, L_kv / block_size]."""
+    bsattn_create_layout_rect; block_mask is then [L / block_size, L_kv / block_size].
+    A 3-D block_mask [H, nb, nb_kv] gives each head its own mask (BSATTN_MASK_PER_HEAD)."""
     m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
+    if m.ndim == 3:
+        if m.shape[0] != H:
+            raise ValueError(f"a per-head block_mask needs {H} masks, got {m.shape[0]}")
+        flags |= BSATTN_MASK_PER_HEAD
     h = ctypes.c_void_p()
     if L_kv is None or L_kv == L:
         st = load().bsattn_create_layout(ctypes.byref(h), B, H, L, D, block_size, m.ctypes.data, flags)
@@ -310,13 +316,15 @@ def bsattn_layout_info(lay: Layout) -> LayoutInfo:
 
 
 def bsattn_layout_export(lay: Layout, with_tiles: bool = False):
-    """(row_ptr [nb+1], col_idx [nnz], units [n_units, 4]) as int32 numpy arrays; with_tiles adds
-    (tile_ptr [nb+1], tiles [key_tiles, 2])."""
+    """(row_ptr [mask_heads*nb+1], col_idx [nnz], units [n_units, 4]) as int32 numpy arrays; with_tiles
+    adds (tile_ptr [mask_heads*nb+1], tiles [key_tiles, 2]).  Segment m*nb + qb is query block qb of
+    mask m (m = 0 for a shared mask, the head for per-head masks)."""
     i = lay.info
-    row_ptr = np.zeros(i.nb + 1, np.int32)
+    nseg = max(1, i.mask_heads) * i.nb  # (mask, query block) segments
+    row_ptr = np.zeros(nseg + 1, np.int32)
     col_idx = np.zeros(max(i.nnz_blocks, 1), np.int32)
     units = np.zeros((i.n_units, 4), np.int32)
-    tile_ptr = np.zeros(i.nb + 1, np.int32)
+    tile_ptr = np.zeros(nseg + 1, np.int32)
     tiles = np.zeros((max(i.key_tiles, 1), 2), np.int32)
     _check(load().bsattn_layout_export(lay.handle, row_ptr.ctypes.data, col_idx.ctypes.data, units.ctypes.data,
                                        tile_ptr.ctypes.data, tiles.ctypes.data), "bsattn_layout_export")

@@ -29,12 +29,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     const int32_t nb = lay.nb;
     const int32_t nbkv = lay.nbkv;
-    lay.row_ptr.assign(static_cast<size_t>(nb) + 1, 0);
+    const int32_t nseg = lay.mask_heads * nb;  // (mask, query block) segments
+    lay.row_ptr.assign(static_cast<size_t>(nseg) + 1, 0);
     lay.col_idx.clear();
-    for (int32_t qb = 0; qb < nb; ++qb) {
+    for (int32_t sg = 0; sg < nseg; ++sg) {
         for (int32_t kb = 0; kb < nbkv; ++kb)
-            if (mask[static_cast<int64_t>(qb) * nbkv + kb]) lay.col_idx.push_back(kb);
-        lay.row_ptr[qb + 1] = static_cast<int32_t>(lay.col_idx.size());
+            if (mask[static_cast<int64_t>(sg) * nbkv + kb]) lay.col_idx.push_back(kb);
+        lay.row_ptr[sg + 1] = static_cast<int32_t>(lay.col_idx.size());
     }
     // Key tiles: the allowed key blocks of a query block, grouped into runs of
     // consecutive frames (contiguous keys, all allowed), each run cut into tiles of
@@ -43,11 +44,11 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     // element mask and no padding, and no tile reaches into a masked frame.
     lay.kv_tile = bsv::kKvTile;
     lay.qt_per_block = (lay.bs + bsv::kQTile - 1) / bsv::kQTile;
-    lay.tile_ptr.assign(static_cast<size_t>(nb) + 1, 0);
+    lay.tile_ptr.assign(static_cast<size_t>(nseg) + 1, 0);
     lay.tiles.clear();
-    for (int32_t qb = 0; qb < nb; ++qb) {
-        int32_t e = lay.row_ptr[qb];
-        const int32_t e1 = lay.row_ptr[qb + 1];
+    for (int32_t sg = 0; sg < nseg; ++sg) {
+        int32_t e = lay.row_ptr[sg];
+        const int32_t e1 = lay.row_ptr[sg + 1];
         while (e < e1) {
             int32_t run_end = e + 1;
             while (run_end < e1 && lay.col_idx[run_end] == lay.col_idx[run_end - 1] + 1) ++run_end;
@@ -59,7 +60,7 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
             }
             e = run_end;
         }
-        lay.tile_ptr[qb + 1] = static_cast<int32_t>(lay.tiles.size() / 2);
+        lay.tile_ptr[sg + 1] = static_cast<int32_t>(lay.tiles.size() / 2);
     }
 
     // Cost model (in hundredths of a two-tile key tile): a unit of two query tiles takes
@@ -72,9 +73,13 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     std::vector<Unit> us;
     const int32_t BH = lay.B * lay.H;
     us.reserve(static_cast<size_t>(BH) * nb * ((lay.qt_per_block + 1) / 2));
+    int64_t mma_frames = 0, allowed_pairs = 0;  // over the B * H sequences
     for (int32_t bh = 0; bh < BH; ++bh)
         for (int32_t qb = 0; qb < nb; ++qb) {
-            const int64_t ntile = lay.tile_ptr[qb + 1] - lay.tile_ptr[qb];
+            const int sg = bsv::plan_segment(lay.mask_heads, lay.H, nb, bh, qb);
+            const int64_t ntile = lay.tile_ptr[sg + 1] - lay.tile_ptr[sg];
+            allowed_pairs += lay.row_ptr[sg + 1] - lay.row_ptr[sg];
+            mma_frames += lay.row_ptr[sg + 1] > lay.row_ptr[sg] ? 1 : 0;
             for (int32_t qt0 = 0; qt0 < lay.qt_per_block; qt0 += 2) {
                 const int32_t nt = std::min(2, lay.qt_per_block - qt0);
                 us.push_back({bh, qb, qt0, nt, ntile * (nt == 2 ? 100 : 83) + 150});
@@ -93,11 +98,9 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
         lay.units[4 * i + 3] = us[i].nt;
         lay.unit_cost[i] = us[i].cost;
     }
-    int64_t reading_frames = 0;
-    for (int32_t qb = 0; qb < nb; ++qb) reading_frames += lay.row_ptr[qb + 1] > lay.row_ptr[qb] ? 1 : 0;
-    lay.mma_rows = static_cast<int64_t>(BH) * reading_frames * lay.qt_per_block * bsv::kQTile;
-    lay.useful_flop = 4.0 * static_cast<double>(lay.col_idx.size()) * static_cast<double>(lay.bs) *
-                      static_cast<double>(lay.bs) * lay.D * lay.H * lay.B;
+    lay.mma_rows = mma_frames * lay.qt_per_block * bsv::kQTile;
+    lay.useful_flop =
+        4.0 * static_cast<double>(allowed_pairs) * static_cast<double>(lay.bs) * static_cast<double>(lay.bs) * lay.D;
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver once (no link-time libcuda dependency).
@@ -273,7 +276,7 @@ bsattn_status bsattn_create_layout_rect(bsattn_layout_t *out, int32_t B, int32_t
     if (!out) return BSATTN_ERR_INVALID_ARG;
     *out = nullptr;
     if (!block_mask || B < 1 || H < 1 || L < 1 || L_kv < 1 || block_size < 1) return BSATTN_ERR_INVALID_ARG;
-    if ((flags & ~BSATTN_PLAN_ONLY) != 0) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~(BSATTN_PLAN_ONLY | BSATTN_MASK_PER_HEAD)) != 0) return BSATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
     if (block_size % 16 != 0 || L % block_size != 0 || L_kv % block_size != 0) return BSATTN_ERR_UNALIGNED_BLOCK;
     const int64_t nb = L / block_size, nbkv = L_kv / block_size;
@@ -292,6 +295,7 @@ bsattn_status bsattn_create_layout_rect(bsattn_layout_t *out, int32_t B, int32_t
         lay->bs = block_size;
         lay->nb = static_cast<int32_t>(nb);
         lay->nbkv = static_cast<int32_t>(nbkv);
+        lay->mask_heads = (flags & BSATTN_MASK_PER_HEAD) ? H : 1;
         lay->plan_only = (flags & BSATTN_PLAN_ONLY) != 0;
         build_plan(*lay, block_mask);
     } catch (const std::bad_alloc &) {
@@ -333,6 +337,8 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
     p.nb = lay->nb;
     p.nbkv = lay->nbkv;
     p.BH = lay->B * lay->H;
+    p.heads = lay->H;
+    p.mask_heads = lay->mask_heads;
     p.chunks_per_block = (lay->bs + bsv::bounds_chunk_rows() - 1) / bsv::bounds_chunk_rows();
     p.scale = scale;
     cudaError_t e = cudaMemsetAsync(kmax, 0, static_cast<size_t>(p.BH) * lay->nbkv * 4, s);
@@ -372,6 +378,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.tiles = lay->d_tiles;
     p.n_tiles = static_cast<int32_t>(lay->tiles.size() / 2);
     p.bh = lay->B * lay->H;
+    p.heads = lay->H;
+    p.mask_heads = lay->mask_heads;
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
@@ -469,6 +477,7 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
     info->useful_flop = lay->useful_flop;
     info->L_kv = lay->Lkv;
     info->nb_kv = lay->nbkv;
+    info->mask_heads = lay->mask_heads;
     return BSATTN_OK;
 }
 

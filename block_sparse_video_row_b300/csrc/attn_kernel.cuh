@@ -138,7 +138,8 @@ __device__ __forceinline__ bool fetch_unit_checked(const AttnParams &p, int i, i
             ok = U.x >= 0 && U.x < p.bh && U.y >= 0 && U.y < p.nb && U.z >= 0 &&
                  (static_cast<int64_t>(U.z) + U.w - 1) * kQTile < p.block;
             if (ok) {
-                const int a = p.tile_ptr[U.y], b = p.tile_ptr[U.y + 1];
+                const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+                const int a = p.tile_ptr[sg], b = p.tile_ptr[sg + 1];
                 ok = a >= 0 && a <= b && b <= p.n_tiles;
                 for (int t = a; ok && t < b; ++t) {
                     int2 T = p.tiles[t];
@@ -390,7 +391,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 int u;
                 int4 U;
                 if (!fetch_unit(p, i, u, U, true)) continue;  // rejected by the device checks
-                const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
+                const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+                const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
                 if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
                 // testing only: the first unit's query tiles are never loaded, so the
                 // issuers' bounded waits run out and the CTA aborts and returns
@@ -477,7 +479,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 int u;
                 int4 U;
                 if (!fetch_unit(p, i, u, U, false)) continue;  // rejected by the device checks
-                const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
+                const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+                const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
                 if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
                 if (t >= U.w) {
                     // This query tile is absent from the unit: release each stage without MMAs,
@@ -573,7 +576,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!fetch_unit(p, i, u, U, false)) continue;  // rejected by the device checks
             const int nt = U.w;
             if (nt == 0) continue;  // an empty schedule slot
-            const int t0 = p.tile_ptr[U.y], nkv = p.tile_ptr[U.y + 1] - t0;
+            const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+            const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
             const int64_t row0 = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
                                  static_cast<int64_t>(U.z) * kQTile + r;  // this thread's row of tile 0
             const bool valid0 = r < min(kQTile, p.block - U.z * kQTile);

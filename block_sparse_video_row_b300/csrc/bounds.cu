@@ -127,8 +127,9 @@ __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsPara
     const int64_t bh = seg / p.nb;
     __shared__ float kB;
     if (threadIdx.x == 0) {
+        const int sg = plan_segment(p.mask_heads, p.heads, p.nb, bh, qb);
         float m = 0.0f;
-        for (int e = p.row_ptr[qb]; e < p.row_ptr[qb + 1]; ++e) {
+        for (int e = p.row_ptr[sg]; e < p.row_ptr[sg + 1]; ++e) {
             const float x = __uint_as_float(p.kmax_bits[bh * p.nbkv + p.col_idx[e]]);
             m = x > m ? x : m;
         }

@@ -10,7 +10,8 @@
 // waits for chunk c-2's copy-out (the output it overwrites).  The call is ordered
 // after earlier work on the caller's stream, and the caller's stream waits for
 // its last copy-out.  Every chunk is an ordinary forward on a layout of shape
-// (1, G, L, D) with the same mask, so the results are those of bsattn_forward.
+// (1, G, L, D) with the same mask (with one mask per head: the masks of the
+// chunk's heads), so the results are those of bsattn_forward.
 #include <algorithm>
 #include <cmath>
 #include <new>
@@ -23,8 +24,9 @@
 namespace bsv {
 
 struct HostPipe {
-    int32_t G = 0, G_last = 0;  // pairs per chunk; pairs of the last chunk
-    bsattn_layout_t sub_full = nullptr, sub_last = nullptr;
+    int32_t G = 0, G_last = 0;             // pairs per chunk; pairs of the last chunk
+    std::vector<bsattn_layout_t> chunk;    // the layout each chunk runs on
+    std::vector<bsattn_layout_t> owned;    // the distinct chunk layouts
     cudaStream_t s_in = nullptr, s_cmp = nullptr, s_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_done = nullptr;
     cudaEvent_t ev_in[2] = {}, ev_cmp[2] = {}, ev_out[2] = {};
@@ -49,8 +51,7 @@ void host_pipe_destroy(HostPipe *hp) {
     if (hp->ev_done) cudaEventDestroy(hp->ev_done);
     for (cudaStream_t s : {hp->s_in, hp->s_cmp, hp->s_out})
         if (s) cudaStreamDestroy(s);
-    bsattn_destroy(hp->sub_full);
-    bsattn_destroy(hp->sub_last);
+    for (bsattn_layout_t sub : hp->owned) bsattn_destroy(sub);
     delete hp;
 }
 
@@ -76,14 +77,59 @@ bsattn_status host_pipe_create(const bsattn_layout_s &lay, int32_t G, HostPipe *
     const int32_t BH = lay.B * lay.H;
     hp->G = G;
     hp->G_last = BH - (BH - 1) / G * G;
-    std::vector<uint8_t> mask(static_cast<size_t>(lay.nb) * lay.nbkv, 0);
-    for (int32_t qb = 0; qb < lay.nb; ++qb)
-        for (int32_t e = lay.row_ptr[qb]; e < lay.row_ptr[qb + 1]; ++e)
-            mask[static_cast<size_t>(qb) * lay.nbkv + lay.col_idx[e]] = 1;
-    bsattn_status st =
-        bsattn_create_layout_rect(&hp->sub_full, 1, G, lay.L, lay.Lkv, lay.D, lay.bs, mask.data(), 0);
-    if (st == BSATTN_OK && hp->G_last != G)
-        st = bsattn_create_layout_rect(&hp->sub_last, 1, hp->G_last, lay.L, lay.Lkv, lay.D, lay.bs, mask.data(), 0);
+    // The masks, rebuilt from the plan: [mask_heads][nb][nbkv].
+    const size_t per_mask = static_cast<size_t>(lay.nb) * lay.nbkv;
+    std::vector<uint8_t> mask;
+    try {
+        mask.assign(static_cast<size_t>(lay.mask_heads) * per_mask, 0);
+    } catch (const std::bad_alloc &) {
+        host_pipe_destroy(hp);
+        return BSATTN_ERR_OOM;
+    }
+    for (int32_t sg = 0; sg < lay.mask_heads * lay.nb; ++sg)
+        for (int32_t e = lay.row_ptr[sg]; e < lay.row_ptr[sg + 1]; ++e)
+            mask[static_cast<size_t>(sg) * lay.nbkv + lay.col_idx[e]] = 1;
+    // Chunk c holds pairs c*G .. c*G + g - 1; pair p is head p % H.  With a shared mask
+    // every chunk of g pairs runs on the same layout; with one mask per head, chunks
+    // whose first head and size agree do.
+    const int32_t nc = (BH + G - 1) / G;
+    std::vector<std::pair<int64_t, bsattn_layout_t>> made;
+    std::vector<uint8_t> sub_mask;
+    bsattn_status st = BSATTN_OK;
+    try {
+        hp->chunk.reserve(static_cast<size_t>(nc));
+        hp->owned.reserve(static_cast<size_t>(nc));
+        made.reserve(static_cast<size_t>(nc));
+        sub_mask.reserve(static_cast<size_t>(G) * per_mask * (lay.mask_heads > 1 ? 1 : 0));
+    } catch (const std::bad_alloc &) {
+        host_pipe_destroy(hp);
+        return BSATTN_ERR_OOM;
+    }
+    for (int32_t c = 0; c < nc && st == BSATTN_OK; ++c) {
+        const int32_t g = c == nc - 1 ? hp->G_last : G;
+        const int32_t h0 = lay.mask_heads > 1 ? static_cast<int32_t>((static_cast<int64_t>(c) * G) % lay.H) : 0;
+        const int64_t key = static_cast<int64_t>(h0) * (BH + 1) + g;
+        bsattn_layout_t sub = nullptr;
+        for (const auto &m : made)
+            if (m.first == key) sub = m.second;
+        if (!sub) {
+            const uint8_t *mk = mask.data();
+            int32_t fl = 0;
+            if (lay.mask_heads > 1) {
+                sub_mask.resize(static_cast<size_t>(g) * per_mask);
+                for (int32_t i = 0; i < g; ++i)
+                    std::copy_n(mask.data() + static_cast<size_t>((h0 + i) % lay.H) * per_mask, per_mask,
+                                sub_mask.data() + static_cast<size_t>(i) * per_mask);
+                mk = sub_mask.data();
+                fl = BSATTN_MASK_PER_HEAD;
+            }
+            st = bsattn_create_layout_rect(&sub, 1, g, lay.L, lay.Lkv, lay.D, lay.bs, mk, fl);
+            if (st != BSATTN_OK) break;
+            made.push_back({key, sub});
+            hp->owned.push_back(sub);
+        }
+        hp->chunk.push_back(sub);
+    }
     if (st != BSATTN_OK) {
         host_pipe_destroy(hp);
         return st;
@@ -154,7 +200,7 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
     for (int32_t c = 0; c < nc && e == cudaSuccess; ++c) {
         const int b = c & 1;
         const int32_t g = c == nc - 1 ? hp.G_last : G;
-        bsattn_layout_t sub = g == G ? hp.sub_full : hp.sub_last;
+        bsattn_layout_t sub = hp.chunk[c];
         const size_t off_q = static_cast<size_t>(c) * G * pair_q, off_kv = static_cast<size_t>(c) * G * pair_kv;
         const size_t bytes_q = static_cast<size_t>(g) * pair_q * 2, bytes_kv = static_cast<size_t>(g) * pair_kv * 2;
         const size_t rows = static_cast<size_t>(g) * lay->L;

@@ -42,6 +42,8 @@ struct AttnParams {
     const int2 *tiles;        // (first key within the head, width: a multiple of 16, <= kKvTile)
     int32_t n_tiles;          // entries of tiles
     int32_t bh;               // B * H
+    int32_t heads;            // H
+    int32_t mask_heads;       // block masks: 1 (shared by all heads) or H (mask h for head h)
     const float *rowbound;    // [B*H*L]
     uint16_t *o;              // [B*H*L, D] bf16 bits
     float *lse;               // [B*H*L] or null
@@ -67,9 +69,16 @@ struct BoundsParams {
     const int32_t *row_ptr, *col_idx;
     int64_t L, Lkv;           // query / key tokens per sequence
     int32_t block, nb, nbkv, BH;
+    int32_t heads, mask_heads; // H; block masks: 1 (shared) or H (mask h for head h)
     int32_t chunks_per_block; // row chunks per frame block
     float scale;
 };
+
+// Segment of the plan's tables (row_ptr, tile_ptr) for query block qb of sequence bh
+// (= b * H + h): mask m = h of a per-head plan (0 for a shared mask), segment m * nb + qb.
+__host__ __device__ __forceinline__ int plan_segment(int mask_heads, int heads, int nb, int64_t bh, int qb) {
+    return (mask_heads > 1 ? static_cast<int>(bh % heads) * nb : 0) + qb;
+}
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s);

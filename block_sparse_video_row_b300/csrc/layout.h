@@ -24,6 +24,7 @@ struct bsattn_layout_s {
     int64_t L = 0;                                // query tokens per sequence
     int32_t nbkv = 0;                             // key blocks
     int64_t Lkv = 0;                              // key tokens per sequence
+    int32_t mask_heads = 1;                       // block masks: 1 (shared) or H (one per head)
     bool plan_only = false;
     std::vector<int32_t> row_ptr, col_idx, units;
     std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs

@@ -149,6 +149,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.tiles = reinterpret_cast<const int2 *>(base + off_tiles);
     p.n_tiles = info.key_tiles;
     p.bh = info.B * info.H;
+    p.heads = info.H;
+    p.mask_heads = 1;
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;

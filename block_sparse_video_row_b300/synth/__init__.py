@@ -123,6 +123,13 @@ def dense_mask(nb: int) -> np.ndarray:
     return np.ones((nb, nb), dtype=np.uint8)
 
 
+def mixed_head_masks(nb: int, H: int) -> np.ndarray:
+    """uint8 [H, nb, nb], one mask per head: head h follows rule h % 4 -- window +-1 plus
+    a global first frame, window +-2, its own frame only, every frame."""
+    rules = (window_mask(nb, 1, True), window_mask(nb, 2), window_mask(nb, 0), dense_mask(nb))
+    return np.stack([rules[h % 4] for h in range(H)])
+
+
 # ----------------------------------------------------------------------------------------------
 # the workloads
 
@@ -178,8 +185,12 @@ class Workload:
         return float(np.float32(1.0 / np.sqrt(self.D)))
 
     def block_mask(self) -> np.ndarray:
-        """uint8 [nq, frames]: the last nq rows of the frames x frames mask."""
-        return np.ascontiguousarray(self.mask(self.frames)[self.frames - self.nq:, :])
+        """uint8 [nq, frames]: the last nq rows of the frames x frames mask ([H, nq, frames]
+        for a workload with one mask per head)."""
+        m = self.mask(self.frames)
+        if m.ndim == 3 and m.shape[0] != self.H:  # fewer or more heads than the masks were made for
+            m = np.stack([m[h % m.shape[0]] for h in range(self.H)])
+        return np.ascontiguousarray(m[..., self.frames - self.nq:, :])
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -203,6 +214,11 @@ WORKLOADS: Dict[str, Workload] = {
     # a streamed 720p chunk: 4 query frames of 3600 tokens reading 9 context frames plus the chunk
     # (window +-1 plus frame 0 over the 13 frames)
     "stream": Workload("stream", 1, 24, 128, 13, 3600, lambda nb: window_mask(nb, 1, True), q_frames=4),
+    # one mask per head (rules cycling over the heads: window +-1 plus frame 0, window +-2,
+    # own frame, every frame) at the small shape, as a streamed chunk, and at 720p
+    "small_heads": Workload("small_heads", 1, 8, 128, 8, 400, lambda nb: mixed_head_masks(nb, 8)),
+    "stream_heads": Workload("stream_heads", 1, 8, 128, 8, 400, lambda nb: mixed_head_masks(nb, 8), q_frames=3),
+    "720p_heads": Workload("720p_heads", 1, 24, 128, 13, 3600, lambda nb: mixed_head_masks(nb, 24)),
 }
 
 
@@ -242,10 +258,12 @@ def make_qkv(w: Workload):
 
 
 def useful_flop(w_or_B, H=None, D=None, block=None, mask=None) -> float:
-    """4 * sum over allowed (q-block, kv-block) pairs of block^2 * D * H * B."""
+    """4 * sum over allowed (q-block, kv-block) pairs of block^2 * D * H * B (a per-head
+    mask [H, nq, nkv] already counts its pairs over the heads)."""
     if isinstance(w_or_B, Workload):
         w = w_or_B
         B, H, D, block, mask = w.B, w.H, w.D, w.block, w.block_mask()
     else:
         B = w_or_B
-    return 4.0 * float(np.count_nonzero(mask)) * block * block * D * H * B
+    heads = 1 if np.ndim(mask) == 3 else H
+    return 4.0 * float(np.count_nonzero(mask)) * block * block * D * heads * B

@@ -116,7 +116,10 @@ enum {
     BSATTN_DEBUG_PLANT_INDEX = 0x400,
     /* bsattn_create_layout: build the host plan only, touch no device; such a
        layout can be inspected (info/export) but not run. */
-    BSATTN_PLAN_ONLY = 0x10
+    BSATTN_PLAN_ONLY = 0x10,
+    /* bsattn_create_layout(_rect): one block mask per head.  block_mask then holds
+       H masks, [H][nb][nb_kv] bytes, and head h of every batch reads mask h. */
+    BSATTN_MASK_PER_HEAD = 0x20
 };
 
 /* Eligibility of a row for the bound softmax, in nats: rows with a larger
@@ -138,8 +141,9 @@ enum {
  *   L           tokens per sequence (frames x tokens per frame), a multiple of block_size.
  *   D           head dimension: 64 or 128.
  *   block_size  tokens per frame block: a multiple of 16 (>= 16).
- *   block_mask  host pointer, nb * nb bytes, nb = L / block_size.
- *   flags       0, or BSATTN_PLAN_ONLY.
+ *   block_mask  host pointer, nb * nb bytes, nb = L / block_size (row-major by query
+ *               block, 1 = attend); H * nb * nb bytes with BSATTN_MASK_PER_HEAD.
+ *   flags       0, or BSATTN_PLAN_ONLY and/or BSATTN_MASK_PER_HEAD.
  * The plan: the allowed key blocks of each query block in ascending order;
  * the key tiles of each query block (its allowed blocks grouped into runs of
  * consecutive frames, each run cut into tiles of 128 keys and one last tile of
@@ -158,8 +162,9 @@ bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, i
 
 /*
  * The same for a streamed chunk: L query tokens (the chunk) reading L_kv >= L key
- * tokens (context frames and the chunk; L_kv < L returns BSATTN_ERR_UNSUPPORTED).  block_mask is nb * nb_kv bytes,
- * nb = L / block_size, nb_kv = L_kv / block_size, row-major by query block.
+ * tokens (context frames and the chunk; L_kv < L returns BSATTN_ERR_UNSUPPORTED).  block_mask is nb * nb_kv bytes
+ * (H * nb * nb_kv with BSATTN_MASK_PER_HEAD), nb = L / block_size, nb_kv = L_kv / block_size, row-major by
+ * query block.
  * Q and O are [B, H, L, D], K and V [B, H, L_kv, D], qnorm and rowbound
  * [B, H, L], kmax [B, H, nb_kv].  bsattn_create_layout(..., L, ...) equals
  * bsattn_create_layout_rect(..., L, L, ...).  Returns as bsattn_create_layout.
@@ -298,26 +303,29 @@ bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, in
 typedef struct {
     int32_t B, H, D, block_size, nb;
     int64_t L;
-    int32_t nnz_blocks;        /* allowed (query block, key block) pairs */
+    int32_t nnz_blocks;        /* allowed (query block, key block) pairs, summed over the masks */
     int32_t kv_tile;           /* keys per full key tile (128) */
-    int32_t key_tiles;         /* key tiles over all query blocks */
+    int32_t key_tiles;         /* key tiles over all query blocks of all masks */
     int32_t q_tiles_per_block; /* ceil(block_size / 128) */
     int32_t n_units;           /* work units (pairs of query tiles of one frame) */
     int64_t mma_rows;          /* query rows the MMAs process, partial tiles included */
-    double useful_flop;        /* 4 * nnz_blocks * block_size^2 * D * H * B */
+    double useful_flop;        /* 4 * block_size^2 * D * B * (allowed pairs summed over the H heads) */
     int64_t L_kv;              /* key tokens per sequence (L for self-attention) */
     int32_t nb_kv;             /* key blocks */
+    int32_t mask_heads;        /* masks in the plan: 1, or H with BSATTN_MASK_PER_HEAD */
 } bsattn_layout_info_t;
 
 bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info);
 
 /*
- * Copy the plan to host arrays (any may be NULL):
- *   row_ptr  int32 [nb + 1], col_idx int32 [nnz_blocks]: allowed key blocks per query block, ascending;
+ * Copy the plan to host arrays (any may be NULL).  Query block qb of mask m is
+ * segment s = m * nb + qb (m = 0 for a shared mask; m = h with BSATTN_MASK_PER_HEAD):
+ *   row_ptr  int32 [mask_heads * nb + 1], col_idx int32 [nnz_blocks]: allowed key blocks of
+ *            segment s in col_idx[row_ptr[s] .. row_ptr[s+1]), ascending;
  *   units    int32 [n_units * 4]: (b * H + h, query block, first query tile, tiles in the unit (1 or 2)),
  *            in execution order;
- *   tile_ptr int32 [nb + 1], tiles int32 [key_tiles * 2]: the key tiles of query block qb are
- *            (tiles[2t], tiles[2t+1]) = (first key within the head, width) for t in [tile_ptr[qb], tile_ptr[qb+1]).
+ *   tile_ptr int32 [mask_heads * nb + 1], tiles int32 [key_tiles * 2]: the key tiles of segment s are
+ *            (tiles[2t], tiles[2t+1]) = (first key within the head, width) for t in [tile_ptr[s], tile_ptr[s+1]).
  */
 bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units,
                                    int32_t *tile_ptr, int32_t *tiles);

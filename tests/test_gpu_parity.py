@@ -107,7 +107,7 @@ def full_case(ba, q, k, v, mask, bs, scale, flags=0, what=""):
 # ------------------------------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("name", ["tiny", "small", "stream_small"])
+@pytest.mark.parametrize("name", ["tiny", "small", "stream_small", "small_heads", "stream_heads"])
 def test_workload_full(ba, name):
     w = synth.WORKLOADS[name]
     q, k, v = synth.make_qkv(w)
@@ -267,6 +267,19 @@ def test_streamed_chunk_equals_last_rows_of_the_full_window(ba):
                           full["rowbound"][:, :, w.L_kv - w.L:].view(np.uint32))
 
 
+def test_per_head_plan_with_equal_masks_equals_the_shared_plan(ba):
+    # One mask per head, every head given the shared mask: the same key tiles for every
+    # row, so the per-head plan reproduces the shared plan's output bit for bit.
+    w = synth.WORKLOADS["small"]
+    q, k, v = synth.make_qkv(w)
+    mask = w.block_mask()
+    shared = run_gpu(ba, q, k, v, mask, w.block, w.scale, want_meta=True)
+    per_head = run_gpu(ba, q, k, v, np.stack([mask] * w.H), w.block, w.scale, want_meta=True)
+    assert torch.equal(shared["o_raw"].view(torch.int16), per_head["o_raw"].view(torch.int16))
+    assert np.array_equal(shared["rowbound"].view(np.uint32), per_head["rowbound"].view(np.uint32))
+    assert per_head["status"] == 0
+
+
 def test_deterministic(ba):
     w = synth.WORKLOADS["small"]
     q, k, v = synth.make_qkv(w)
@@ -276,7 +289,7 @@ def test_deterministic(ba):
 
 
 @pytest.mark.parametrize("name,heads", [("720p", [0, 7, 23]), ("stress", [0, 11]), ("1080p", [5]),
-                                        ("stream", [0, 13])])
+                                        ("stream", [0, 13]), ("720p_heads", [0, 1, 2, 3, 22])])
 def test_workload_sampled(ba, name, heads):
     w = synth.WORKLOADS[name]
     q, k, v = synth.make_qkv(w)
@@ -313,7 +326,8 @@ def _pinned(x):
 
 
 @pytest.mark.parametrize("name,pairs,flags", [("small", 3, 0), ("small", 0, 1), ("tiny", 1, 4),
-                                              ("stream_small", 3, 0)])
+                                              ("stream_small", 3, 0), ("small_heads", 3, 0),
+                                              ("stream_heads", 0, 0)])
 def test_host_path_equals_device_path(ba, name, pairs, flags):
     # bsattn_forward_host (pinned host tensors, chunked copies and kernels on three streams)
     # against bsattn_forward on device copies: the same kernels per row, so identical bits.
@@ -367,7 +381,7 @@ def _mid_case():
     return q, k, v, synth.window_mask(nf, 1), bs, 1.0 / np.sqrt(D)
 
 
-@pytest.mark.parametrize("name", ["tiny", "small", "stream_small", "mid"])
+@pytest.mark.parametrize("name", ["tiny", "small", "stream_small", "small_heads", "mid"])
 def test_device_checks_accept_valid_plans_and_change_nothing(ba, name):
     # BSATTN_DEBUG_CHECKS on a valid plan: no unit rejected (status stays ok) and the
     # output is bit-identical to the unchecked launch.

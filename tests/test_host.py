@@ -55,15 +55,23 @@ def check_tiles(mask, bs, tile_ptr, tiles):
 def test_plan_matches_oracle(lib, name):
     w = synth.WORKLOADS[name]
     mask = w.block_mask()
+    masks = mask if mask.ndim == 3 else mask[None]  # per-head plans: segment m * nb + qb is mask m
     lay = bsattn.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, bsattn.BSATTN_PLAN_ONLY, L_kv=w.L_kv)
     info = lay.info
+    assert info.mask_heads == len(masks)
     row_ptr, col_idx, units, tile_ptr, tiles = bsattn.bsattn_layout_export(lay, with_tiles=True)
-    orp, oci = oracle.allowed_csr(mask)
+    orp, oci = [0], []
+    for m in masks:
+        rp, ci = oracle.allowed_csr(m)
+        orp += list(rp[1:] + orp[-1])
+        oci += list(ci)
     assert np.array_equal(row_ptr, orp) and np.array_equal(col_idx, oci)
     assert info.nnz_blocks == len(oci) and info.nb == w.nb
     assert info.L == w.L and info.L_kv == w.L_kv and info.nb_kv == w.nb_kv
     assert info.kv_tile == 128 and info.key_tiles == len(tiles)
-    check_tiles(mask, w.block, tile_ptr, tiles)
+    for mi, m in enumerate(masks):
+        seg = tile_ptr[mi * w.nb:(mi + 1) * w.nb + 1]
+        check_tiles(m, w.block, seg, tiles)
     nqt = -(-w.block // 128)
     assert info.q_tiles_per_block == nqt
     assert abs(info.useful_flop - synth.useful_flop(w)) == 0
@@ -75,7 +83,8 @@ def test_plan_matches_oracle(lib, name):
     assert np.all(seen == 1)
     # largest cost first, by the documented model: 100 per key tile for a unit of two query
     # tiles, 83 for one tile, plus 150 per unit
-    ntile = np.diff(tile_ptr)[units[:, 1]]
+    segment = (units[:, 0] % w.H if len(masks) > 1 else 0) * w.nb + units[:, 1]
+    ntile = np.diff(tile_ptr)[segment]
     cost = ntile * np.where(units[:, 3] == 2, 100, 83) + 150
     assert np.all(np.diff(cost) <= 0)
     lay.destroy()

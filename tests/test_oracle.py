@@ -349,16 +349,21 @@ def test_norm_recipe_vs_fp64_and_bounds():
 def test_workload_sizes_golden():
     g = json.load(open(GOLDEN))["workloads"]
     for name, w in synth.WORKLOADS.items():
-        row_ptr, col_idx = oracle.allowed_csr(w.block_mask())
-        assert len(col_idx) == g[name]["nnz"], name
+        mask = w.block_mask()
+        masks = mask if mask.ndim == 3 else mask[None]  # one mask per head, or one for all
+        csrs = [oracle.allowed_csr(m) for m in masks]
+        assert sum(len(c) for _, c in csrs) == g[name]["nnz"], name
+        if mask.ndim == 3:
+            assert len(masks) == w.H
         assert (w.B, w.H, w.D, w.frames, w.block) == (g[name]["B"], g[name]["H"], g[name]["D"],
                                                        g[name]["frames"], g[name]["block"])
         assert w.nq == g[name].get("q_frames", g[name]["frames"])
         assert synth.useful_flop(w) == g[name]["useful_flop"]
         # ascending within each query block
-        for qb in range(w.nb):
-            s = col_idx[row_ptr[qb]:row_ptr[qb + 1]]
-            assert np.all(np.diff(s) > 0)
+        for row_ptr, col_idx in csrs:
+            for qb in range(w.nb):
+                s = col_idx[row_ptr[qb]:row_ptr[qb + 1]]
+                assert np.all(np.diff(s) > 0)
 
 
 def test_generator_matches_splitmix64_definition():
