@@ -271,6 +271,10 @@ def bsattn_forward_noalloc(q, k, v, o, B: int, H: int, L: int, D: int, block_siz
     """The forward without a layout, for callers that may not allocate device memory
     (see bsattn_forward_noalloc in include/bsattn.h)."""
     m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
+    if m.ndim == 3:
+        if m.shape[0] != H:
+            raise ValueError(f"a per-head block_mask needs {H} masks, got {m.shape[0]}")
+        flags |= BSATTN_MASK_PER_HEAD
     n = B * H * L
     for name, x in (("q", q), ("k", k), ("v", v), ("o", o)):
         _check_arg(name, x, n * D, 2, True)

@@ -73,7 +73,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
                                                 int32_t H, int64_t L, int32_t D, int32_t block_size,
                                                 const uint8_t *block_mask, float scale, const float *rowbound,
                                                 float *lse, int32_t flags, bsattn_stream_t stream) {
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY)) != 0) return BSATTN_ERR_INVALID_ARG;
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_MASK_PER_HEAD)) != 0)
+        return BSATTN_ERR_INVALID_ARG;
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
     const auto mis16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) != 0; };
@@ -90,7 +91,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
 
     // The work plan, built on the host only (the plan-only layout touches no device).
     bsattn_layout_t plan = nullptr;
-    bsattn_status st = bsattn_create_layout(&plan, B, H, L, D, block_size, block_mask, BSATTN_PLAN_ONLY);
+    bsattn_status st = bsattn_create_layout(&plan, B, H, L, D, block_size, block_mask,
+                                            BSATTN_PLAN_ONLY | (flags & BSATTN_MASK_PER_HEAD));
     if (st != BSATTN_OK) return st;
     bsattn_layout_info_t info;
     bsattn_layout_info(plan, &info);
@@ -103,7 +105,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     // work.
     const size_t off_units = align256((8 + 2 * n) * 4);
     const size_t off_tileptr = align256(off_units + 16 * n);
-    const size_t off_tiles = align256(off_tileptr + 4 * (static_cast<size_t>(info.nb) + 1));
+    const size_t off_tiles =
+        align256(off_tileptr + 4 * (static_cast<size_t>(info.mask_heads) * static_cast<size_t>(info.nb) + 1));
     const size_t total = off_tiles + 8 * ntiles;
     if (total > kNoallocScratchBytes) {
         bsattn_destroy(plan);
@@ -150,7 +153,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.n_tiles = info.key_tiles;
     p.bh = info.B * info.H;
     p.heads = info.H;
-    p.mask_heads = 1;
+    p.mask_heads = info.mask_heads;
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;

@@ -258,7 +258,8 @@ bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q, const void
  * or library routine.
  *   q, k, v, o, scale, rowbound, lse, flags: as for bsattn_forward (device pointers;
  *             rowbound from bsattn_row_bounds or any equal bound).
- *   B, H, L, D, block_size, block_mask: as for bsattn_create_layout (mask on the host).
+ *   B, H, L, D, block_size, block_mask: as for bsattn_create_layout (mask on the host; with
+ *             BSATTN_MASK_PER_HEAD in flags, one mask per head).
  * Limits: the plan (work units x 24 bytes + the key-tile table, 8 bytes per
  * tile, each part rounded up to 256 bytes) must fit in the array, about 40,000
  * work units (the 720p chunk uses 4,680, the 1080p chunk 9,984); a larger

@@ -83,6 +83,14 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(ba):
     assert np.all(np.isfinite(got)) and err.max() <= O_MAX and err.mean() <= O_MEAN
 
 
+def test_noalloc_with_one_mask_per_head(ba):
+    w, q, k, v = _case("small_heads")
+    ref, got, fb_rows = _both(ba, w, q, k, v, ba.BSATTN_BOUND)
+    assert fb_rows == 0
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)) and err.max() <= O_MAX and err.mean() <= O_MEAN
+
+
 def test_noalloc_rejects_plans_beyond_its_array(ba):
     # 512 heads of the 720p shape: ~100k work units, more than the 1 MiB array holds.
     # The check comes before any device work, so the pointers are never dereferenced.
