@@ -165,6 +165,29 @@ def test_streamed_edge_shapes(ba, D, B, H, nq, nkv, bs):
     full_case(ba, q, k, v, mask, bs, scale, what=f"stream {B}x{H} {nq}/{nkv}x{bs} D{D}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B,H,nq,nkv,bs", [
+    (2, 3, 3, 3, 48),     # self-attention, several batches (head h of every batch reads mask h)
+    (1, 4, 2, 5, 272),    # streamed chunk, three query tiles per frame, 16-row tail
+])
+def test_per_head_edge_shapes(ba, D, B, H, nq, nkv, bs):
+    # One random mask per head, one head with a query frame that reads nothing: every
+    # row against the oracle, metadata bit-exact.
+    rng = np.random.default_rng(H * 10 + nkv)
+    masks = (rng.random((H, nq, nkv)) < 0.5).astype(np.uint8)
+    masks[:, np.arange(nq), nkv - nq + np.arange(nq)] = 1  # every frame reads its own frame ...
+    masks[1, 0, :] = 0                                     # ... except frame 0 under head 1's mask
+    q = synth.tensor_bf16(6, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(6, synth.TAG_K, B, H, nkv * bs, D)
+    v = synth.tensor_bf16(6, synth.TAG_V, B, H, nkv * bs, D)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    res = full_case(ba, q, k, v, masks, bs, scale, what=f"per-head {B}x{H} {nq}/{nkv}x{bs} D{D}")
+    L = nq * bs
+    rows = np.arange(B * H * L)
+    empty = ((rows // L) % H == 1) & ((rows % L) // bs == 0)
+    assert np.all(res["o"][empty] == 0) and np.all(np.isneginf(res["lse"][empty]))
+
+
 @pytest.mark.parametrize("flags", [1, 2, 4, 6])
 def test_variants_small(ba, flags):
     w = synth.WORKLOADS["small"]
