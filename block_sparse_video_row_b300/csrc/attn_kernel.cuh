@@ -16,7 +16,8 @@
 //
 // One CTA per SM processes work units: a unit is one or two 128-row query tiles
 // of the same frame (they share every K/V tile), looping over the frame's key
-// tiles.  The host deals the units to the CTAs (slot k * gridDim + c is CTA c's
+// tiles (under its head's own mask when the layout has one mask per head, found
+// through plan_segment).  The host deals the units to the CTAs (slot k * gridDim + c is CTA c's
 // k-th unit; empty slots have no query tiles and are skipped).  Query rows index
 // Q and O over L tokens per head, keys index K and V over L_kv >= L (a streamed
 // chunk reads context frames before its own).
