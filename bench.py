@@ -21,6 +21,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -56,7 +57,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples go to $BSATTN_CLOCKS_DIR (kept) or the temp directory
+        d = os.environ.get("BSATTN_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"bsattn_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         try:
