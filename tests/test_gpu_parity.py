@@ -188,6 +188,26 @@ def test_per_head_edge_shapes(ba, D, B, H, nq, nkv, bs):
     assert np.all(res["o"][empty] == 0) and np.all(np.isneginf(res["lse"][empty]))
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes(ba, seed):
+    # Random small problems: head dim, batch, heads, frame size (a multiple of 16), query
+    # and key frame counts, and a random mask (shared or one per head, streamed or not);
+    # every row against the oracle, metadata bit-exact.
+    rng = np.random.default_rng(1000 + seed)
+    D = int(rng.choice([64, 128]))
+    B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+    bs = 16 * int(rng.integers(1, 20))
+    nkv = int(rng.integers(1, 7))
+    nq = nkv if rng.random() < 0.5 else int(rng.integers(1, nkv + 1))
+    shape = (H, nq, nkv) if rng.random() < 0.5 else (nq, nkv)
+    mask = (rng.random(shape) < 0.6).astype(np.uint8)
+    q = synth.tensor_bf16(2000 + seed, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(2000 + seed, synth.TAG_K, B, H, nkv * bs, D)
+    v = synth.tensor_bf16(2000 + seed, synth.TAG_V, B, H, nkv * bs, D)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    full_case(ba, q, k, v, mask, bs, scale, what=f"random {seed}: D{D} {B}x{H} {nq}/{nkv}x{bs} mask{shape}")
+
+
 @pytest.mark.parametrize("flags", [1, 2, 4, 6])
 def test_variants_small(ba, flags):
     w = synth.WORKLOADS["small"]

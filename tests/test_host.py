@@ -252,3 +252,35 @@ def test_header_is_plain_c_and_a_c_client_links_and_runs(lib, tmp_path):
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0, run.stdout + run.stderr
     assert run.stdout.strip() == "nb=4 nnz=10 units=8 row_ptr_last=10 refs=11"
+
+
+def test_plan_matches_oracle_on_random_masks(lib):
+    # Random shapes and masks (shared, streamed and per head, some rows empty): the plan's
+    # CSR equals the oracle's per mask, and the key tiles cover exactly the allowed keys.
+    rng = np.random.default_rng(2024)
+    for trial in range(60):
+        bs = int(rng.choice([16, 48, 128, 144, 272, 400]))
+        nbkv = int(rng.integers(1, 9))
+        nb = int(rng.integers(1, nbkv + 1))
+        H = int(rng.integers(1, 5))
+        per_head = bool(rng.integers(0, 2))
+        shape = (H, nb, nbkv) if per_head else (nb, nbkv)
+        mask = (rng.random(shape) < rng.uniform(0.1, 0.9)).astype(np.uint8)
+        lay = bsattn.bsattn_create_layout(2, H, nb * bs, 64, bs, mask, bsattn.BSATTN_PLAN_ONLY, L_kv=nbkv * bs)
+        row_ptr, col_idx, units, tile_ptr, tiles = bsattn.bsattn_layout_export(lay, with_tiles=True)
+        masks = mask if per_head else mask[None]
+        assert lay.info.mask_heads == len(masks)
+        orp, oci = [0], []
+        for m in masks:
+            rp, ci = oracle.allowed_csr(m)
+            orp += list(rp[1:] + orp[-1])
+            oci += list(ci)
+        assert np.array_equal(row_ptr, orp) and np.array_equal(col_idx, oci), trial
+        for mi, m in enumerate(masks):
+            check_tiles(m, bs, tile_ptr[mi * nb:(mi + 1) * nb + 1], tiles)
+        nqt = -(-bs // 128)
+        seen = np.zeros((2 * H, nb, nqt), np.int32)
+        for bh, qb, qt0, nt in units:
+            seen[bh, qb, qt0:qt0 + nt] += 1
+        assert np.all(seen == 1), trial
+        lay.destroy()
