@@ -61,6 +61,13 @@ extern "C" {
  * default 4000 ms), records BSATTN_ERR_TIMEOUT in the layout's status word and
  * returns, so a stalled pipeline never hangs the GPU. */
 
+/* Concurrency: a layout holds one guard workspace (counters, unit flags, fallback
+ * list), reset by every bsattn_forward, and bsattn_forward_host keeps its staging,
+ * streams and chunk layouts in the layout.  Calls on one layout must therefore be
+ * ordered: issue them on one stream (or order the streams with events) and from one
+ * host thread at a time.  Use one layout per concurrent stream.  Different layouts are
+ * independent. */
+
 /* A cudaStream_t, passed through unchanged (NULL = the legacy default stream). */
 typedef struct CUstream_st *bsattn_stream_t;
 
