@@ -200,30 +200,34 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
     return pk;
 }
 
-// S columns [tS, tS + w), w a multiple of 16 and at most 64: two TMEM loads of 32
-// columns, the second in flight while the first is converted.  P of the first 32
+// S columns [tS, tS + w), w a multiple of 16 and at most 64, in buf: two TMEM loads of
+// 32 columns, the second in flight while the first is converted -- or, with PRE, S is
+// already in buf (loaded by load_half_max on the running-max path).  P of the first 32
 // keys goes to columns [tS, tS + 16) and of the next 32 to [tS + 16, tS + 32): both
-// were loaded by then, and the load in flight reads columns >= tS + 32.  mid() runs
-// once the first group's P is stored (its P.V MMAs may then start), whatever w is.
-template <typename Mid>
+// were loaded by then, and a load in flight reads columns >= tS + 32.  mid() runs once
+// the first group's P is stored (its P.V MMAs may then start), whatever w is.
+template <bool PRE, typename Mid>
 __device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, uint64_t nm2x2, float (&l)[4],
-                                             Mid &&mid) {
+                                             uint32_t (&buf)[2][32], Mid &&mid) {
     if (w <= 0) {
         mid();
         return;
     }
-    uint32_t buf[2][32];
-    if (w >= 32)
-        tmem_ld32(tS, buf[0]);
-    else
-        tmem_ld16_into32(tS, buf[0]);
+    if (!PRE) {
+        if (w >= 32)
+            tmem_ld32(tS, buf[0]);
+        else
+            tmem_ld16_into32(tS, buf[0]);
+    }
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         if (32 * g < w) {
             const bool full = w - 32 * g >= 32;
-            tmem_wait_ld();
-            reg_fence32(buf[g]);
-            if (g == 0 && w > 32) {
+            if (!PRE) {
+                tmem_wait_ld();
+                reg_fence32(buf[g]);
+            }
+            if (!PRE && g == 0 && w > 32) {
                 if (w >= 64)
                     tmem_ld32(tS + 32, buf[1]);
                 else
@@ -251,25 +255,31 @@ __device__ __forceinline__ void softmax_half(uint32_t tS, int w, uint64_t c1x2, 
     }
 }
 
-// Row max of S columns [tS, tS + w) (raw logits), for the online-max variant; -inf if w == 0.
-__device__ __forceinline__ float half_row_max(uint32_t tS, int w) {
+// For the running-max path: S columns [tS, tS + w) loaded once into buf (both groups
+// of 32, the second possibly of 16) and their maximum returned (raw logits; -inf if
+// w == 0); softmax_half<true> then converts the same registers.
+__device__ __forceinline__ float load_half_max(uint32_t tS, int w, uint32_t (&buf)[2][32]) {
     float mx = -INFINITY;
+    if (w <= 0) return mx;
+    if (w >= 32)
+        tmem_ld32(tS, buf[0]);
+    else
+        tmem_ld16_into32(tS, buf[0]);
+    if (w >= 64)
+        tmem_ld32(tS + 32, buf[1]);
+    else if (w > 32)
+        tmem_ld16_into32(tS + 32, buf[1]);
+    tmem_wait_ld();
+    reg_fence32(buf[0]);
+    if (w > 32) reg_fence32(buf[1]);
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         if (32 * g < w) {
-            uint32_t a[32];
-            const bool full = w - 32 * g >= 32;
-            if (full)
-                tmem_ld32(tS + 32 * g, a);
-            else
-                tmem_ld16_into32(tS + 32 * g, a);
-            tmem_wait_ld();
-            reg_fence32(a);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
-            if (full) {
+            for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(buf[g][e]));
+            if (w - 32 * g >= 32) {
 #pragma unroll
-                for (int e = 16; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
+                for (int e = 16; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(buf[g][e]));
             }
         }
     }
@@ -632,10 +642,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t tS = t ? tS1 : tS0;
                     float(&lt)[4] = t ? lt1 : lt0;
                     uint64_t &nm = t ? nm1 : nm0;
+                    // S of this half: loaded here for the running max (and kept for P), or by
+                    // softmax_half on the bound path.
+                    uint32_t sbuf[2][32];
                     if (t ? on1 : on0) {
                         float &mrow = t ? mrow1 : mrow0;
                         float other;
-                        const float mine = half_row_max(tS, wh) * c1;
+                        const float mine = load_half_max(tS, wh, sbuf) * c1;
                         ok = pair_exchange(bar, q, h, r, x_uses, mine, other, status, tmo);
                         if (!ok) break;
                         const float mx = fmaxf(mine, other);
@@ -657,12 +670,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     // p_full[t]: the P of every warp's first 32 keys is stored (P.V k-steps 0, 1,
                     // 4, 5 may start); p_rest[t]: all of it is.
-                    softmax_half(tS, wh, c1x2, nm, lt, [&]() {
+                    const auto handoff = [&]() {
                         tmem_wait_st();
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar.p_full + t);
-                    });
+                    };
+                    if (t ? on1 : on0)
+                        softmax_half<true>(tS, wh, c1x2, nm, lt, sbuf, handoff);
+                    else
+                        softmax_half<false>(tS, wh, c1x2, nm, lt, sbuf, handoff);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
