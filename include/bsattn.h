@@ -26,7 +26,8 @@
  * base addresses, on the device that was current at layout creation.  Row i of
  * head (b, h) belongs to block i / block_size, key j to block j / block_size.
  * The block mask is one [nb, nb_kv] uint8 matrix (row-major, nonzero = query
- * block qb reads key block kb), shared by every batch entry and head.
+ * block qb reads key block kb), shared by every batch entry and head, or, with
+ * BSATTN_MASK_PER_HEAD, one such matrix per head (shared by the batch entries).
  * Self-attention over one chunk has L_kv = L (bsattn_create_layout); a streamed
  * chunk whose queries also read earlier context frames has L_kv > L
  * (bsattn_create_layout_rect; the pages stream their output chunk by chunk,
@@ -44,7 +45,8 @@
  *
  * Errors: argument errors are returned before any work is enqueued.  Device-
  * side conditions (a bounded wait that ran out, which the kernel reports and
- * returns from instead of hanging) are recorded in a device status word that
+ * returns from instead of hanging; with BSATTN_DEBUG_CHECKS, a work unit that the
+ * device checks rejected) are recorded in a device status word that
  * bsattn_query_stats returns.
  */
 #ifndef BSATTN_H
