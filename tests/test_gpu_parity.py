@@ -215,6 +215,14 @@ def test_variants_small(ba, flags):
     full_case(ba, q, k, v, w.block_mask(), w.block, w.scale, flags=flags, what=f"small flags={flags}")
 
 
+@pytest.mark.parametrize("flags", [1, 4])
+def test_variants_per_head(ba, flags):
+    # the online-max kernel and the bound-only path on one mask per head
+    w = synth.WORKLOADS["stream_heads"]
+    q, k, v = synth.make_qkv(w)
+    full_case(ba, q, k, v, w.block_mask(), w.block, w.scale, flags=flags, what=f"stream_heads flags={flags}")
+
+
 def _scaled_key(w, factor):
     q, k, v = synth.make_qkv(w)
     k = k.copy()

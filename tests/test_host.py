@@ -284,3 +284,21 @@ def test_plan_matches_oracle_on_random_masks(lib):
             seen[bh, qb, qt0:qt0 + nt] += 1
         assert np.all(seen == 1), trial
         lay.destroy()
+
+
+def test_binding_constants_match_the_header():
+    # Every BSATTN_* enum value and numeric #define in include/bsattn.h has the same value in
+    # the Python binding (no drift between the C ABI and its binding).
+    src = open(os.path.join(ROOT, "include", "bsattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    vals = {}
+    for name, v in re.findall(r"\b(BSATTN_[A-Z_]+)\s*=\s*(0x[0-9A-Fa-f]+|\d+)", src):
+        vals[name] = int(v, 0)
+    for name, v in re.findall(r"#define\s+(BSATTN_[A-Z_]+)\s+([0-9.]+)f?\b", src):
+        vals[name] = float(v)
+    assert len(vals) > 15
+    for name, v in vals.items():
+        if name.startswith("BSATTN_MAX_") or name == "BSATTN_NOALLOC_SCRATCH_BYTES":
+            continue
+        assert hasattr(bsattn, name), name
+        assert getattr(bsattn, name) == v, (name, getattr(bsattn, name), v)
