@@ -366,6 +366,42 @@ def test_workload_sizes_golden():
                 assert np.all(np.diff(s) > 0)
 
 
+def _golden_allowed(g, w, h):
+    """The hand-typed allowed key frames of each query frame under head h's mask."""
+    if "allowed" in g:
+        return g["allowed"]
+    return g["allowed_by_rule"][str(h % 4)]
+
+
+def test_allowed_csr_per_query_block_golden():
+    # The allowed-block sets of every workload, typed by hand from the mask rules
+    # ("HeyGen Avatar IV on Trillium TPU" deep-dive, section 把 block 縮到 16: the mask
+    # decides per frame block which key frames a query frame reads).  The first-frame-
+    # global masks are not symmetric, so a transposed reading of the mask, a row_ptr
+    # shifted by one block or a dropped block fails here.
+    g = json.load(open(GOLDEN))["workloads"]
+    for name, w in synth.WORKLOADS.items():
+        mask = w.block_mask()
+        masks = mask if mask.ndim == 3 else mask[None]
+        for h, m in enumerate(masks):
+            want = _golden_allowed(g[name], w, h)
+            assert len(want) == w.nq, name
+            row_ptr, col_idx = oracle.allowed_csr(m)
+            assert list(row_ptr) == list(np.cumsum([0] + [len(a) for a in want])), (name, h)
+            for qb, a in enumerate(want):
+                assert list(col_idx[row_ptr[qb]:row_ptr[qb + 1]]) == a, (name, h, qb)
+
+
+def test_allowed_csr_rectangular_by_hand():
+    # 3 query blocks reading 4 key blocks; the CSR written out by hand.
+    m = np.array([[1, 0, 0, 1],
+                  [0, 0, 0, 0],
+                  [0, 1, 1, 1]], np.uint8)
+    row_ptr, col_idx = oracle.allowed_csr(m)
+    assert list(row_ptr) == [0, 2, 2, 5]
+    assert list(col_idx) == [0, 3, 1, 2, 3]
+
+
 def test_generator_matches_splitmix64_definition():
     # published SplitMix64 outputs for state 1234567
     assert [synth.splitmix64_at(1234567, i) for i in range(3)] == [
