@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbsattn.so")
-SOURCES = ["api.cpp", "bounds.cu", "attn_d64.cu", "attn_d128.cu", "noalloc.cu", "host_pipeline.cu"]
+SOURCES = ["api.cpp", "bounds.cu", "route.cu", "attn_d64.cu", "attn_d128.cu", "noalloc.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

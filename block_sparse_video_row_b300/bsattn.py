@@ -41,9 +41,11 @@ BSATTN_ELIGIBLE_BOUND = 64.0
 BSATTN_PLAN_ONLY = 0x10
 BSATTN_MASK_PER_HEAD = 0x20
 
-EXPORTED = ("bsattn_create_layout", "bsattn_create_layout_rect", "bsattn_row_bounds", "bsattn_forward", "bsattn_destroy",
-            "bsattn_status_string", "bsattn_query_stats", "bsattn_layout_info", "bsattn_layout_export",
-            "bsattn_forward_noalloc", "bsattn_forward_host")
+EXPORTED = ("bsattn_create_layout", "bsattn_create_layout_rect", "bsattn_row_bounds",
+            "bsattn_row_bounds_from_norms", "bsattn_forward", "bsattn_destroy",
+            "bsattn_status_string", "bsattn_query_stats", "bsattn_query_eligibility", "bsattn_layout_info",
+            "bsattn_layout_export", "bsattn_layout_schedule",
+            "bsattn_forward_noalloc", "bsattn_noalloc_query", "bsattn_forward_host")
 
 
 class LayoutInfo(ctypes.Structure):
@@ -83,6 +85,8 @@ def load(path: Optional[str] = None):
     lib.bsattn_create_layout_rect.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i64, i32, i32, vp, i32]
     lib.bsattn_row_bounds.restype = i32
     lib.bsattn_row_bounds.argtypes = [vp, vp, vp, f32, vp, vp, vp, vp]
+    lib.bsattn_row_bounds_from_norms.restype = i32
+    lib.bsattn_row_bounds_from_norms.argtypes = [vp, vp, vp, f32, vp, vp, vp]
     lib.bsattn_forward.restype = i32
     lib.bsattn_forward.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i32, vp]
     lib.bsattn_destroy.restype = None
@@ -91,12 +95,18 @@ def load(path: Optional[str] = None):
     lib.bsattn_status_string.argtypes = [i32]
     lib.bsattn_query_stats.restype = i32
     lib.bsattn_query_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i32), vp]
+    lib.bsattn_query_eligibility.restype = i32
+    lib.bsattn_query_eligibility.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64), vp]
     lib.bsattn_layout_info.restype = i32
     lib.bsattn_layout_info.argtypes = [vp, ctypes.POINTER(LayoutInfo)]
     lib.bsattn_forward_noalloc.restype = i32
     lib.bsattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, i32, vp, f32, vp, vp, i32, vp]
+    lib.bsattn_noalloc_query.restype = i32
+    lib.bsattn_noalloc_query.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i32), vp]
     lib.bsattn_forward_host.restype = i32
     lib.bsattn_forward_host.argtypes = [vp, vp, vp, vp, vp, f32, vp, i32, i32, vp]
+    lib.bsattn_layout_schedule.restype = i32
+    lib.bsattn_layout_schedule.argtypes = [vp, i32, vp, ctypes.POINTER(i32)]
     lib.bsattn_layout_export.restype = i32
     lib.bsattn_layout_export.argtypes = [vp, vp, vp, vp, vp, vp]
     _lib = lib
@@ -254,6 +264,19 @@ def bsattn_row_bounds(lay: Layout, q, k, scale: float, qnorm, kmax, rowbound, st
     return st
 
 
+def bsattn_row_bounds_from_norms(lay: Layout, qnorm, knorm, scale: float, kmax, rowbound, stream=None,
+                                 raise_on_error: bool = True) -> int:
+    if lay.handle:
+        i = lay.info
+        _check_io(lay, True, rows=(("qnorm", qnorm), ("rowbound", rowbound)), kmax=kmax)
+        _check_arg("knorm", knorm, i.B * i.H * i.L_kv, 4, True)
+    st = load().bsattn_row_bounds_from_norms(lay.handle, _ptr(qnorm), _ptr(knorm), float(scale), _ptr(kmax),
+                                             _ptr(rowbound), _stream(stream))
+    if raise_on_error:
+        _check(st, "bsattn_row_bounds_from_norms")
+    return st
+
+
 def bsattn_forward(lay: Layout, q, k, v, o, scale: float, rowbound, lse=None, flags: int = 0, stream=None,
                    raise_on_error: bool = True) -> int:
     if lay.handle:
@@ -313,10 +336,37 @@ def bsattn_query_stats(lay: Layout, stream=None):
     return rows.value, units.value, dev.value
 
 
+def bsattn_query_eligibility(lay: Layout, stream=None):
+    """(bound_units, online_units) of the last forward's eligibility check; synchronises the stream."""
+    b, o = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().bsattn_query_eligibility(lay.handle, ctypes.byref(b), ctypes.byref(o), _stream(stream)),
+           "bsattn_query_eligibility")
+    return b.value, o.value
+
+
+def bsattn_noalloc_query(stream=None):
+    """(fallback_rows, fallback_units, device_status) of the last bsattn_forward_noalloc on the
+    current device; synchronises the stream and allocates nothing."""
+    rows, units, dev = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    _check(load().bsattn_noalloc_query(ctypes.byref(rows), ctypes.byref(units), ctypes.byref(dev), _stream(stream)),
+           "bsattn_noalloc_query")
+    return rows.value, units.value, dev.value
+
+
 def bsattn_layout_info(lay: Layout) -> LayoutInfo:
     info = LayoutInfo()
     _check(load().bsattn_layout_info(lay.handle, ctypes.byref(info)), "bsattn_layout_info")
     return info
+
+
+def bsattn_layout_schedule(lay: Layout, grid: int) -> np.ndarray:
+    """int32 [n_slots, 4]: slot k * grid + c is CTA c's k-th unit (empty slots are zeros)."""
+    n = ctypes.c_int32()
+    _check(load().bsattn_layout_schedule(lay.handle, grid, None, ctypes.byref(n)), "bsattn_layout_schedule")
+    out = np.zeros((n.value, 4), dtype=np.int32)
+    _check(load().bsattn_layout_schedule(lay.handle, grid, out.ctypes.data, ctypes.byref(n)),
+           "bsattn_layout_schedule")
+    return out
 
 
 def bsattn_layout_export(lay: Layout, with_tiles: bool = False):

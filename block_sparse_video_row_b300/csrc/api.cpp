@@ -25,6 +25,7 @@ bsattn_status from_cuda(cudaError_t e) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
     const int32_t nb = lay.nb;
@@ -85,9 +86,7 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
                 us.push_back({bh, qb, qt0, nt, ntile * (nt == 2 ? 100 : 83) + 150});
             }
         }
-    // Largest first (longest-processing-time order for the persistent CTAs); equal
-    // costs keep (head, frame, tile) order so concurrently running CTAs share K/V in L2.
-    std::stable_sort(us.begin(), us.end(), [](const Unit &a, const Unit &b) { return a.cost > b.cost; });
+    // Units stay in (head, frame, tile) order; schedule_units orders and deals them.
     lay.n_units = static_cast<int32_t>(us.size());
     lay.units.resize(us.size() * 4);
     lay.unit_cost.resize(us.size());
@@ -180,7 +179,7 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
     lay.grid = std::max(1, std::min(lay.n_units, lay.num_sms));
     std::vector<int32_t> slots;
     lay.n_slots = bsv::schedule_units(lay, lay.grid, slots);
-    const size_t ws_ints = kWsHeader + 2 * static_cast<size_t>(lay.n_slots);
+    const size_t ws_ints = kWsHeader + 3 * static_cast<size_t>(lay.n_slots);
     if ((e = cudaMalloc(&lay.d_row_ptr, lay.row_ptr.size() * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_col_idx, nnz * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_tile_ptr, lay.tile_ptr.size() * 4)) != cudaSuccess ||
@@ -206,11 +205,7 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
         free_device(&lay);
         return from_cuda(e);
     }
-    lay.ws.status = lay.d_ws + 0;
-    lay.ws.fb_count = lay.d_ws + 4;
-    lay.ws.fb_rows = lay.d_ws + 5;
-    lay.ws.unit_flag = lay.d_ws + kWsHeader;
-    lay.ws.fb_list = lay.d_ws + kWsHeader + lay.n_slots;
+    lay.ws = bsv::workspace_at(lay.d_ws, lay.n_slots);
 
     uint64_t ms = 4000;
     if (const char *env = std::getenv("BSATTN_TIMEOUT_MS")) {
@@ -219,6 +214,29 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
     }
     lay.timeout_ns = ms * 1000000ull;
     return BSATTN_OK;
+}
+
+// Parameters of the bound kernels for a layout (Q and K pointers left null).
+bsv::BoundsParams bounds_params(const bsattn_layout_s &lay, float scale, float *qnorm, float *kmax, float *rowbound) {
+    bsv::BoundsParams p;
+    p.q = nullptr;
+    p.k = nullptr;
+    p.qnorm = qnorm;
+    p.kmax_bits = reinterpret_cast<uint32_t *>(kmax);
+    p.rowbound = rowbound;
+    p.row_ptr = lay.d_row_ptr;
+    p.col_idx = lay.d_col_idx;
+    p.L = lay.L;
+    p.Lkv = lay.Lkv;
+    p.block = lay.bs;
+    p.nb = lay.nb;
+    p.nbkv = lay.nbkv;
+    p.BH = lay.B * lay.H;
+    p.heads = lay.H;
+    p.mask_heads = lay.mask_heads;
+    p.chunks_per_block = (lay.bs + bsv::bounds_chunk_rows() - 1) / bsv::bounds_chunk_rows();
+    p.scale = scale;
+    return p;
 }
 
 bsattn_status check_runnable(const bsattn_layout_s *lay) {
@@ -231,8 +249,22 @@ bsattn_status check_runnable(const bsattn_layout_s *lay) {
 }  // namespace
 
 namespace bsv {
+// Units of the schedule's cost-sorted tail, in waves of G (one unit per CTA).
+constexpr int32_t kTailWaves = 4;
+
 int32_t schedule_units(const bsattn_layout_s &lay, int32_t G, std::vector<int32_t> &slots) {
     G = std::max(1, G);
+    // Deal order: the plan's (head, frame, tile) order, so that the CTAs running at any
+    // one time work on one or two heads and find each K/V tile in L2 after its first read
+    // (a head's K and V take 1.8 MB per 3600-token frame); then the last kTailWaves * G
+    // units by cost, largest first (ties keep plan order), so small units fill the end
+    // and the CTAs finish together.
+    const int32_t n = lay.n_units;
+    std::vector<int32_t> order(static_cast<size_t>(n));
+    for (int32_t u = 0; u < n; ++u) order[u] = u;
+    const int64_t tail = std::min<int64_t>(n, static_cast<int64_t>(kTailWaves) * G);
+    std::stable_sort(order.begin() + (n - tail), order.end(),
+                     [&](int32_t a, int32_t b) { return lay.unit_cost[a] > lay.unit_cost[b]; });
     std::vector<std::vector<int32_t>> per(static_cast<size_t>(G));
     std::vector<int64_t> load(static_cast<size_t>(G), 0);
     // least-loaded CTA first (ties: lowest index), units in cost order
@@ -241,7 +273,7 @@ int32_t schedule_units(const bsattn_layout_s &lay, int32_t G, std::vector<int32_
     for (int32_t c = 0; c < G; ++c) heap.push_back({0, c});
     auto cmp = [](const Entry &a, const Entry &b) { return a.first != b.first ? a.first > b.first : a.second > b.second; };
     std::make_heap(heap.begin(), heap.end(), cmp);
-    for (int32_t u = 0; u < lay.n_units; ++u) {
+    for (int32_t u : order) {
         std::pop_heap(heap.begin(), heap.end(), cmp);
         Entry &e = heap.back();
         per[e.second].push_back(u);
@@ -318,31 +350,31 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
     bsattn_status st = check_runnable(lay);
     if (st != BSATTN_OK) return st;
     if (!q || !k || !qnorm || !kmax || !rowbound) return BSATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(qnorm) & 3) ||
-        (reinterpret_cast<uintptr_t>(kmax) & 3) || (reinterpret_cast<uintptr_t>(rowbound) & 3))
+    if (!aligned16(q) || !aligned16(k) || !aligned4(qnorm) || !aligned4(kmax) || !aligned4(rowbound))
         return BSATTN_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    bsv::BoundsParams p;
+    bsv::BoundsParams p = bounds_params(*lay, scale, qnorm, kmax, rowbound);
     p.q = static_cast<const uint16_t *>(q);
     p.k = static_cast<const uint16_t *>(k);
-    p.qnorm = qnorm;
-    p.kmax_bits = reinterpret_cast<uint32_t *>(kmax);
-    p.rowbound = rowbound;
-    p.row_ptr = lay->d_row_ptr;
-    p.col_idx = lay->d_col_idx;
-    p.L = lay->L;
-    p.Lkv = lay->Lkv;
-    p.block = lay->bs;
-    p.nb = lay->nb;
-    p.nbkv = lay->nbkv;
-    p.BH = lay->B * lay->H;
-    p.heads = lay->H;
-    p.mask_heads = lay->mask_heads;
-    p.chunks_per_block = (lay->bs + bsv::bounds_chunk_rows() - 1) / bsv::bounds_chunk_rows();
-    p.scale = scale;
     cudaError_t e = cudaMemsetAsync(kmax, 0, static_cast<size_t>(p.BH) * lay->nbkv * 4, s);
     if (e == cudaSuccess) e = bsv::launch_norms(p, lay->D, s);
+    if (e == cudaSuccess) e = bsv::launch_rowbound(p, s);
+    return from_cuda(e);
+}
+
+bsattn_status bsattn_row_bounds_from_norms(bsattn_layout_t lay, const float *qnorm, const float *knorm, float scale,
+                                           float *kmax, float *rowbound, bsattn_stream_t stream) {
+    bsattn_status st = check_runnable(lay);
+    if (st != BSATTN_OK) return st;
+    if (!qnorm || !knorm || !kmax || !rowbound) return BSATTN_ERR_INVALID_ARG;
+    if (!aligned4(qnorm) || !aligned4(knorm) || !aligned4(kmax) || !aligned4(rowbound)) return BSATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the row-bound kernel only reads qnorm
+    bsv::BoundsParams p = bounds_params(*lay, scale, const_cast<float *>(qnorm), kmax, rowbound);
+    cudaError_t e = cudaMemsetAsync(kmax, 0, static_cast<size_t>(p.BH) * lay->nbkv * 4, s);
+    if (e == cudaSuccess) e = bsv::launch_kmax_from_norms(p, knorm, s);
     if (e == cudaSuccess) e = bsv::launch_rowbound(p, s);
     return from_cuda(e);
 }
@@ -367,8 +399,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     if (!encode_q_map(&tq, *lay, q) || !encode_kv_map(&tk, *lay, k) || !encode_kv_map(&tv, *lay, v))
         return BSATTN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // per-call part of the workspace: fb_count, fb_rows and the unit flags
-    cudaError_t e = cudaMemsetAsync(lay->d_ws + 4, 0, (kWsHeader - 4 + static_cast<size_t>(lay->n_slots)) * 4, s);
+    // per-call counters of the workspace header: fb_count, fb_rows, n_online, n_bound
+    cudaError_t e = cudaMemsetAsync(lay->d_ws + 4, 0, (kWsHeader - 4) * 4, s);
     if (e != cudaSuccess) return from_cuda(e);
 
     bsv::AttnParams p;
@@ -403,6 +435,10 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
         p.mode = bsv::kModeOnlineAll;
         return from_cuda(launch(true));
     }
+    // the eligibility check of every unit, then the bound launch over the eligible ones
+    // and the online launch over the others and the guard's fallback list
+    e = bsv::launch_route(p, s);
+    if (e != cudaSuccess) return from_cuda(e);
     p.mode = bsv::kModeBound;
     e = launch(false);
     if (e != cudaSuccess) return from_cuda(e);
@@ -460,6 +496,20 @@ bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, in
     return BSATTN_OK;
 }
 
+bsattn_status bsattn_query_eligibility(bsattn_layout_t lay, int64_t *bound_units, int64_t *online_units,
+                                      bsattn_stream_t stream) {
+    bsattn_status st = check_runnable(lay);
+    if (st != BSATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    int32_t h[kWsHeader];
+    e = cudaMemcpy(h, lay->d_ws, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (online_units) *online_units = h[6];
+    if (bound_units) *bound_units = h[7];
+    return BSATTN_OK;
+}
+
 bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info) {
     if (!lay || !info) return BSATTN_ERR_INVALID_ARG;
     info->B = lay->B;
@@ -478,6 +528,18 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
     info->L_kv = lay->Lkv;
     info->nb_kv = lay->nbkv;
     info->mask_heads = lay->mask_heads;
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_layout_schedule(bsattn_layout_t lay, int32_t grid, int32_t *slots, int32_t *n_slots) {
+    if (!lay || !n_slots || grid < 1) return BSATTN_ERR_INVALID_ARG;
+    std::vector<int32_t> v;
+    try {
+        *n_slots = bsv::schedule_units(*lay, grid, v);
+    } catch (const std::bad_alloc &) {
+        return BSATTN_ERR_OOM;
+    }
+    if (slots && !v.empty()) std::memcpy(slots, v.data(), v.size() * 4);
     return BSATTN_OK;
 }
 

@@ -118,18 +118,31 @@ __device__ __forceinline__ Bars carve_bars(uint8_t *base, uint8_t *xchg) {
     return r;
 }
 
-__device__ __forceinline__ int unit_index(const AttnParams &p, int i) {
-    return p.mode == kModeFallback ? p.ws.fb_list[i] : i;
+// Sequence position i of this launch -> schedule slot.  The fallback launch first walks
+// the schedule (positions below `base`, where base = n_units when the route kernel sent
+// units to it, else 0), then the guard's fallback list.
+__device__ __forceinline__ int unit_index(const AttnParams &p, int i, int base) {
+    return (p.mode == kModeFallback && i >= base) ? p.ws.fb_list[i - base] : i;
+}
+
+// Whether schedule position i is this launch's work: the bound launch takes the slots
+// the route kernel left bound, the fallback launch the ones it routed online (and every
+// fallback-list entry); the online-max-everywhere launch takes all.
+__device__ __forceinline__ bool slot_for_launch(const AttnParams &p, int i, int base) {
+    if (p.mode == kModeBound) return p.ws.slot_online[i] == 0;
+    if (p.mode == kModeFallback && i < base) return p.ws.slot_online[i] != 0;
+    return true;
 }
 
 // The work unit of slot i, checked (device checks on): false when the slot, the unit
 // (head, query block, each query tile starting inside the frame), its key-tile range
 // or any key tile it reads (16-aligned start, width 16..kKvTile, inside the head's
 // L_kv keys) is out of range.  Reads only what the checks before it allowed.
-__device__ __forceinline__ bool fetch_unit_checked(const AttnParams &p, int i, int &u, int4 &U, bool report) {
-    bool ok = i >= 0 && i < p.n_units;
+__device__ __forceinline__ bool fetch_unit_checked(const AttnParams &p, int i, int base, int &u, int4 &U,
+                                                   bool report) {
+    bool ok = i >= 0 && (p.mode == kModeFallback ? i - base < p.n_units : i < p.n_units);
     if (ok) {
-        u = unit_index(p, i);
+        u = unit_index(p, i, base);
         ok = u >= 0 && u < p.n_units;
     }
     if (ok) {
@@ -160,12 +173,17 @@ __device__ __forceinline__ bool fetch_unit_checked(const AttnParams &p, int i, i
     return ok;
 }
 
-// The work unit of slot i.  With device checks on, false for a unit the checks
-// reject; the caller skips it.  Every role calls this with the same i, so all roles
-// skip the same units; only the caller with `report` records the status bit.
-__device__ __forceinline__ bool fetch_unit(const AttnParams &p, int i, int &u, int4 &U, bool report) {
-    if (p.checks) return fetch_unit_checked(p, i, u, U, report);
-    u = unit_index(p, i);
+// The work unit at sequence position i of this launch.  False for a slot that is not
+// this launch's work (slot_for_launch) and, with device checks on, for a unit the
+// checks reject; the caller skips it.  Every role calls this with the same i, so all
+// roles skip the same units; only the caller with `report` records the status bit.
+__device__ __forceinline__ bool fetch_unit(const AttnParams &p, int i, int base, int &u, int4 &U, bool report) {
+    // (slot_for_launch reads slot_online[i] only where i < n_units: the loops of every
+    // role run i < n_units in the bound launch, and i < base = n_units for the schedule
+    // part of the fallback launch)
+    if (!slot_for_launch(p, i, base)) return false;
+    if (p.checks) return fetch_unit_checked(p, i, base, u, U, report);
+    u = unit_index(p, i, base);
     U = p.units[u];
     return true;
 }
@@ -339,7 +357,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
     using C = AttnCfg<D>;
-    const int n_seq = p.mode == kModeFallback ? *reinterpret_cast<volatile int32_t *>(p.ws.fb_count) : p.n_units;
+    // Positions of this launch: the bound launch walks the schedule unless the route kernel
+    // sent every unit online; the fallback launch walks the schedule when it sent some
+    // (base = n_units), then the guard's fallback list.
+    int n_seq = p.n_units, base = 0;
+    if (p.mode == kModeBound) {
+        if (*reinterpret_cast<volatile int32_t *>(p.ws.n_bound) == 0) n_seq = 0;
+    } else if (p.mode == kModeFallback) {
+        base = *reinterpret_cast<volatile int32_t *>(p.ws.n_online) > 0 ? p.n_units : 0;
+        n_seq = base + *reinterpret_cast<volatile int32_t *>(p.ws.fb_count);
+    }
     if (static_cast<int>(blockIdx.x) >= n_seq) return;  // nothing to do: exit before any TMEM allocation
 
     extern __shared__ uint8_t smem_raw[];
@@ -401,7 +428,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 int u;
                 int4 U;
-                if (!fetch_unit(p, i, u, U, true)) continue;  // rejected by the device checks
+                if (!fetch_unit(p, i, base, u, U, true)) continue;  // not this launch's, or rejected by the checks
                 const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
                 const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
                 if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
@@ -489,7 +516,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
                 int u;
                 int4 U;
-                if (!fetch_unit(p, i, u, U, false)) continue;  // rejected by the device checks
+                if (!fetch_unit(p, i, base, u, U, false)) continue;  // not this launch's, or rejected by the checks
                 const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
                 const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
                 if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
@@ -584,7 +611,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
             int u;
             int4 U;
-            if (!fetch_unit(p, i, u, U, false)) continue;  // rejected by the device checks
+            if (!fetch_unit(p, i, base, u, U, false)) continue;  // not this launch's, or rejected by the checks
             const int nt = U.w;
             if (nt == 0) continue;  // an empty schedule slot
             const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
@@ -606,22 +633,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 continue;
             }
-            // Per query tile, this warp's 32 rows take the bound softmax when all of them
-            // are eligible (bound at most elig_m), else the running max.  The decision is
-            // warp-uniform and equal in both column halves (same rows, same bounds).
-            // mrow: bound m_i (natural units) or the running max (log2 units).
+            // mrow: the bound m_i (natural units) on the bound path; the running max (log2
+            // units) on the online path.  The route kernel sent every unit with a row above
+            // the eligibility limit to the online launch, so each kernel has one path.
             float mrow0, mrow1;
-            bool on0, on1;
             if constexpr (ONLINE) {
-                on0 = on1 = true;
                 mrow0 = mrow1 = -INFINITY;
             } else {
-                const float b0 = valid0 ? p.rowbound[row0] : 0.0f;
-                const float b1 = valid1 ? p.rowbound[row0 + kQTile] : 0.0f;
-                on0 = __any_sync(0xFFFFFFFFu, b0 > p.elig_m);
-                on1 = __any_sync(0xFFFFFFFFu, b1 > p.elig_m);
-                mrow0 = on0 ? -INFINITY : b0;
-                mrow1 = on1 ? -INFINITY : b1;
+                mrow0 = valid0 ? p.rowbound[row0] : 0.0f;
+                mrow1 = valid1 ? p.rowbound[row0 + kQTile] : 0.0f;
             }
             uint64_t nm0 = f2_make(-mrow0 * 1.4426950408889634f, -mrow0 * 1.4426950408889634f);
             uint64_t nm1 = f2_make(-mrow1 * 1.4426950408889634f, -mrow1 * 1.4426950408889634f);
@@ -645,7 +665,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // S of this half: loaded here for the running max (and kept for P), or by
                     // softmax_half on the bound path.
                     uint32_t sbuf[2][32];
-                    if (t ? on1 : on0) {
+                    if constexpr (ONLINE) {
                         float &mrow = t ? mrow1 : mrow0;
                         float other;
                         const float mine = load_half_max(tS, wh, sbuf) * c1;
@@ -676,10 +696,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar.p_full + t);
                     };
-                    if (t ? on1 : on0)
-                        softmax_half<true>(tS, wh, c1x2, nm, lt, sbuf, handoff);
-                    else
-                        softmax_half<false>(tS, wh, c1x2, nm, lt, sbuf, handoff);
+                    softmax_half<ONLINE>(tS, wh, c1x2, nm, lt, sbuf, handoff);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -731,15 +748,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 if (h == 0) {
                     const float mrow = t ? mrow1 : mrow0;
-                    const bool on = t ? on1 : on0;
                     if (valid && p.lse) {
-                        if (on)
+                        if constexpr (ONLINE)
                             p.lse[grow] = (mrow + log2f(l)) * 0.6931471805599453f;
                         else
                             p.lse[grow] = mrow + logf(l);
                     }
                     if constexpr (!ONLINE) {
-                        if (p.mode == kModeBound && !on) {
+                        if (p.mode == kModeBound) {
                             // Underflow guard: a denominator below 2^-64 (or not finite) means the
                             // bound was too loose for exp to resolve this row; rerun its unit with
                             // the online max.

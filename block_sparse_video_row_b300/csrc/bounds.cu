@@ -144,6 +144,45 @@ __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsPara
     }
 }
 
+// kmax from per-token key norms that the caller's producer already wrote (its QK-norm
+// or projection epilogue), so K is not read again: one CTA per row chunk of one key
+// block, one norm per thread, one atomic max per CTA.  Negative and NaN entries lose
+// every comparison against the running maximum, which starts at 0.
+__global__ void __launch_bounds__(kNormThreads) kmax_from_norms_kernel(const BoundsParams p, const float *knorm) {
+    const int cpb = p.chunks_per_block;
+    const int chunk = static_cast<int>(blockIdx.x % cpb);
+    const int64_t seg = blockIdx.x / cpb;  // (b*H + h) * nbkv + kb
+    const int kb = static_cast<int>(seg % p.nbkv);
+    const int64_t bh = seg / p.nbkv;
+    const int nrows = min(kChunkRows, p.block - chunk * kChunkRows);
+    float m = 0.0f;
+    if (static_cast<int>(threadIdx.x) < nrows) {
+        const float x = __ldg(knorm + bh * p.Lkv + static_cast<int64_t>(kb) * p.block +
+                              static_cast<int64_t>(chunk) * kChunkRows + threadIdx.x);
+        m = x > m ? x : m;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+        m = o > m ? o : m;
+    }
+    __shared__ float warp_max[kNormThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float r = warp_max[0];
+#pragma unroll
+        for (int w = 1; w < kNormThreads / 32; ++w) r = warp_max[w] > r ? warp_max[w] : r;
+        atomicMax(p.kmax_bits + seg, __float_as_uint(r));
+    }
+}
+
+cudaError_t launch_kmax_from_norms(const BoundsParams &p, const float *knorm, cudaStream_t s) {
+    const int64_t grid = static_cast<int64_t>(p.BH) * p.nbkv * p.chunks_per_block;
+    kmax_from_norms_kernel<<<static_cast<unsigned>(grid), kNormThreads, 0, s>>>(p, knorm);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s) {
     const int64_t grid = static_cast<int64_t>(p.BH) * p.nbkv * p.chunks_per_block;  // nb <= nbkv
     if (D == 128)

@@ -57,12 +57,12 @@ void host_pipe_destroy(HostPipe *hp) {
 
 namespace {
 
-// Adds a chunk's guard counters into the layout's workspace (slots 0: status bits,
-// 4: units rerun, 5: rows flagged), so bsattn_query_stats reports the whole call.
+// Adds a chunk's counters into the layout's workspace (slots 0: status bits, 4: units
+// rerun, 5: rows flagged, 6: units routed online, 7: units left bound), so
+// bsattn_query_stats and bsattn_query_eligibility report the whole call.
 __global__ void fold_stats_kernel(const int32_t *src, int32_t *dst) {
     dst[0] |= src[0];
-    dst[4] += src[4];
-    dst[5] += src[5];
+    for (int i = 4; i < 8; ++i) dst[i] += src[i];  // guard and eligibility counters
 }
 
 bsattn_status from_cuda(cudaError_t e) {
@@ -196,7 +196,7 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
     for (cudaStream_t s : {hp.s_in, hp.s_cmp, hp.s_out})
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.ev_start, 0);
     // the call's guard counters accumulate in the layout's workspace
-    if (e == cudaSuccess) e = cudaMemsetAsync(lay->d_ws + 4, 0, 2 * sizeof(int32_t), hp.s_cmp);
+    if (e == cudaSuccess) e = cudaMemsetAsync(lay->d_ws + 4, 0, 4 * sizeof(int32_t), hp.s_cmp);
     for (int32_t c = 0; c < nc && e == cudaSuccess; ++c) {
         const int b = c & 1;
         const int32_t g = c == nc - 1 ? hp.G_last : G;

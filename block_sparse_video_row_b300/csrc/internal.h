@@ -20,19 +20,40 @@ constexpr float kGuardTau = 5.421010862427522e-20f;  // 2^-64: smallest denomina
 constexpr int kStatusTimeout = 1;     // bits in the device status word: a bounded wait ran out,
 constexpr int kStatusIndex = 2;       // the device checks rejected a work unit
 
-// Device-side workspace of a layout (one allocation, zeroed per forward where noted).
+// Device-side workspace of a layout (one allocation): an 8-int header, then three
+// arrays of one int per schedule slot.  The header's counters are zeroed per forward
+// (the status word only at create); the route kernel rewrites the per-slot arrays.
 struct Workspace {
-    int32_t *fb_count;   // units appended to the fallback list      (zeroed per forward)
-    int32_t *fb_rows;    // rows flagged by the guard                  (zeroed per forward)
-    int32_t *status;     // device status bits (kStatus*)              (zeroed at create)
-    int32_t *unit_flag;  // per work unit: flagged already             (zeroed per forward)
-    int32_t *fb_list;    // work-unit indices to rerun
+    int32_t *fb_count;     // [4] units appended to the fallback list
+    int32_t *fb_rows;      // [5] rows flagged by the guard
+    int32_t *status;       // [0] device status bits (kStatus*)
+    int32_t *n_online;     // [6] units routed to the online-max launch (eligibility check)
+    int32_t *n_bound;      // [7] units left to the bound-softmax launch
+    int32_t *unit_flag;    // per slot: already appended to the fallback list
+    int32_t *fb_list;      // slot indices to rerun
+    int32_t *slot_online;  // per slot: 1 = a row of the unit is above the eligibility limit
 };
 
+// Workspace views over ws_ints = kWsHeaderInts + 3 * n_slots ints at d.
+constexpr int kWsHeaderInts = 8;
+inline Workspace workspace_at(int32_t *d, int32_t n_slots) {
+    Workspace w;
+    w.status = d + 0;
+    w.fb_count = d + 4;
+    w.fb_rows = d + 5;
+    w.n_online = d + 6;
+    w.n_bound = d + 7;
+    w.unit_flag = d + kWsHeaderInts;
+    w.fb_list = d + kWsHeaderInts + n_slots;
+    w.slot_online = d + kWsHeaderInts + 2 * static_cast<int64_t>(n_slots);
+    return w;
+}
+
 enum AttnMode : int32_t {
-    kModeBound = 0,     // bound softmax over every unit, guard on
+    kModeBound = 0,     // bound softmax over the slots the route kernel left bound, guard on
     kModeOnlineAll = 1, // online max over every unit
-    kModeFallback = 2   // online max over the units listed in fb_list[0 .. *fb_count)
+    kModeFallback = 2   // online max over the slots routed online, then the units listed in
+                        // fb_list[0 .. *fb_count) by the bound launch's guard
 };
 
 struct AttnParams {
@@ -53,7 +74,7 @@ struct AttnParams {
     int32_t block;            // tokens per frame block
     int32_t nb;               // query blocks
     float scale_log2;         // scale * log2(e)
-    float elig_m;             // rows with a larger bound use the online max (kModeBound only)
+    float elig_m;             // route kernel: a unit with a larger row bound goes to the online launch
     int32_t mode;
     int32_t debug_stall;      // testing: skip the first unit's query-tile loads (waits run out)
     int32_t checks;           // device-side index checks of every unit before use
@@ -81,8 +102,14 @@ __host__ __device__ __forceinline__ int plan_segment(int mask_heads, int heads, 
 }
 
 // Launchers (return the launch error, if any).
+// The eligibility check of every schedule slot before the forward's two launches: a
+// unit with a row bound above p.elig_m is routed to the online-max launch; also
+// clears the per-slot guard flags and counts n_online / n_bound (zeroed before).
+cudaError_t launch_route(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s);
 cudaError_t launch_rowbound(const BoundsParams &p, cudaStream_t s);
+// kmax[bh, kb] from caller-supplied key norms knorm [B*H*L_kv] (p.q, p.k unused).
+cudaError_t launch_kmax_from_norms(const BoundsParams &p, const float *knorm, cudaStream_t s);
 int bounds_chunk_rows();
 
 // Attention kernel for head dim D; grid = n_ctas persistent CTAs.

@@ -11,7 +11,8 @@ struct bsattn_layout_s;
 namespace bsv {
 struct HostPipe;                   // staging and streams of bsattn_forward_host (host_pipeline.cu)
 void host_pipe_destroy(HostPipe *hp);
-constexpr int kWsHeader = 8;       // int32 workspace slots: [0] status, [4] fb_count, [5] fb_rows
+constexpr int kWsHeader = kWsHeaderInts;  // int32 workspace header: [0] status, [4] fb_count,
+                                         // [5] fb_rows, [6] n_online, [7] n_bound
 // The per-CTA schedule for a grid of G persistent CTAs: the units, in the layout's
 // cost order, each given to the least-loaded CTA; slot k * G + c holds CTA c's k-th
 // unit (4 int32 each), and empty slots are (0, 0, 0, 0), a unit of no query tiles

@@ -24,6 +24,7 @@
 
 #include "bsattn.h"
 #include "internal.h"
+#include "layout.h"
 
 namespace {
 
@@ -67,13 +68,21 @@ bsattn_status device_setup(int dev, DeviceState **out) {
     return BSATTN_OK;
 }
 
+// Device state of the current device (set-up on first use), or an error.
+bsattn_status current_device(DeviceState **ds) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BSATTN_ERR_DEVICE;
+    return device_setup(dev, ds);
+}
+
 }  // namespace
 
 extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, const void *v, void *o, int32_t B,
                                                 int32_t H, int64_t L, int32_t D, int32_t block_size,
                                                 const uint8_t *block_mask, float scale, const float *rowbound,
                                                 float *lse, int32_t flags, bsattn_stream_t stream) {
-    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_MASK_PER_HEAD)) != 0)
+    if ((flags & ~(BSATTN_ONLINE_MAX | BSATTN_NO_FALLBACK | BSATTN_BOUND_ONLY | BSATTN_MASK_PER_HEAD |
+                   BSATTN_DEBUG_STALL)) != 0)
         return BSATTN_ERR_INVALID_ARG;
     const bool online = (flags & BSATTN_ONLINE_MAX) != 0;
     if (!q || !k || !v || !o || (!online && !rowbound)) return BSATTN_ERR_INVALID_ARG;
@@ -89,21 +98,29 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
         return BSATTN_ERR_CUDA;
     if (capture != cudaStreamCaptureStatusNone) return BSATTN_ERR_UNSUPPORTED;
 
-    // The work plan, built on the host only (the plan-only layout touches no device).
+    // The work plan, built on the host only (the plan-only layout touches no device),
+    // and dealt to one persistent CTA per SM by the same cost model as a device layout,
+    // so the kernels see the same slots as bsattn_forward's.
+    DeviceState *ds = nullptr;
+    bsattn_status st = current_device(&ds);
+    if (st != BSATTN_OK) return st;
     bsattn_layout_t plan = nullptr;
-    bsattn_status st = bsattn_create_layout(&plan, B, H, L, D, block_size, block_mask,
-                                            BSATTN_PLAN_ONLY | (flags & BSATTN_MASK_PER_HEAD));
+    st = bsattn_create_layout(&plan, B, H, L, D, block_size, block_mask,
+                              BSATTN_PLAN_ONLY | (flags & BSATTN_MASK_PER_HEAD));
     if (st != BSATTN_OK) return st;
     bsattn_layout_info_t info;
     bsattn_layout_info(plan, &info);
-    const size_t n = static_cast<size_t>(info.n_units);
+    const int grid = std::max(1, std::min(info.n_units, ds->num_sms));
+    std::vector<int32_t> slots;
+    const int32_t n_slots = bsv::schedule_units(*plan, grid, slots);
+    const size_t n = static_cast<size_t>(n_slots);
     const size_t ntiles = static_cast<size_t>(info.key_tiles > 0 ? info.key_tiles : 1);
 
     // Scratch layout: guard workspace (8 header ints: status, -, -, -, fallback count,
-    // fallback rows, -, -; then per-unit flags; then the fallback list), the work list,
-    // the key-tile table.  Sizes beyond the array are rejected here, before any device
-    // work.
-    const size_t off_units = align256((8 + 2 * n) * 4);
+    // fallback rows, units routed online, units left bound; then per slot a guard flag,
+    // the fallback list and the route), the slots, the key-tile table.  Sizes beyond the
+    // array are rejected here, before any device work.
+    const size_t off_units = align256((bsv::kWsHeaderInts + 3 * n) * 4);
     const size_t off_tileptr = align256(off_units + 16 * n);
     const size_t off_tiles =
         align256(off_tileptr + 4 * (static_cast<size_t>(info.mask_heads) * static_cast<size_t>(info.nb) + 1));
@@ -113,21 +130,10 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
         return BSATTN_ERR_UNSUPPORTED;
     }
     std::vector<unsigned char> host(total, 0);
-    bsattn_layout_export(plan, nullptr, nullptr, reinterpret_cast<int32_t *>(host.data() + off_units),
-                         reinterpret_cast<int32_t *>(host.data() + off_tileptr),
+    std::memcpy(host.data() + off_units, slots.data(), slots.size() * 4);
+    bsattn_layout_export(plan, nullptr, nullptr, nullptr, reinterpret_cast<int32_t *>(host.data() + off_tileptr),
                          reinterpret_cast<int32_t *>(host.data() + off_tiles));
 
-    int dev = -1;
-    DeviceState *ds = nullptr;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        bsattn_destroy(plan);
-        return BSATTN_ERR_DEVICE;
-    }
-    st = device_setup(dev, &ds);
-    if (st != BSATTN_OK) {
-        bsattn_destroy(plan);
-        return st;
-    }
     CUtensorMap tq, tk, tv;
     if (!bsv::encode_layout_maps(plan, q, k, v, &tq, &tk, &tv)) {
         bsattn_destroy(plan);
@@ -147,7 +153,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     int32_t *ws = reinterpret_cast<int32_t *>(base);
     bsv::AttnParams p;
     p.units = reinterpret_cast<const int4 *>(base + off_units);
-    p.n_units = info.n_units;
+    p.n_units = n_slots;
     p.tile_ptr = reinterpret_cast<const int32_t *>(base + off_tileptr);
     p.tiles = reinterpret_cast<const int2 *>(base + off_tiles);
     p.n_tiles = info.key_tiles;
@@ -157,18 +163,14 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.rowbound = rowbound;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
-    p.ws.status = ws + 0;
-    p.ws.fb_count = ws + 4;
-    p.ws.fb_rows = ws + 5;
-    p.ws.unit_flag = ws + 8;
-    p.ws.fb_list = ws + 8 + n;
+    p.ws = bsv::workspace_at(ws, n_slots);
     p.L = L;
     p.Lkv = L;
     p.block = block_size;
     p.nb = info.nb;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.elig_m = (flags & BSATTN_BOUND_ONLY) ? INFINITY : BSATTN_ELIGIBLE_BOUND;
-    p.debug_stall = 0;
+    p.debug_stall = (flags & BSATTN_DEBUG_STALL) ? 1 : 0;
     p.checks = 0;
     p.debug_plant = 0;
     uint64_t ms = 4000;
@@ -177,7 +179,6 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
         if (val > 0) ms = static_cast<uint64_t>(val);
     }
     p.timeout_ns = ms * 1000000ull;
-    const int grid = std::max(1, std::min(info.n_units, ds->num_sms));
     auto launch = [&](bool on) {
         return info.D == 128 ? bsv::launch_attention_d128(tq, tk, tv, p, on, grid, s)
                              : bsv::launch_attention_d64(tq, tk, tv, p, on, grid, s);
@@ -186,9 +187,28 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
         p.mode = bsv::kModeOnlineAll;
         return launch(true) == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
     }
+    if (bsv::launch_route(p, s) != cudaSuccess) return BSATTN_ERR_CUDA;
     p.mode = bsv::kModeBound;
     if (launch(false) != cudaSuccess) return BSATTN_ERR_CUDA;
     if (flags & BSATTN_NO_FALLBACK) return BSATTN_OK;
     p.mode = bsv::kModeFallback;
+    p.debug_stall = 0;
     return launch(true) == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+extern "C" bsattn_status bsattn_noalloc_query(int64_t *fallback_rows, int64_t *fallback_units,
+                                              int32_t *device_status, bsattn_stream_t stream) {
+    DeviceState *ds = nullptr;
+    bsattn_status st = current_device(&ds);
+    if (st != BSATTN_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BSATTN_ERR_CUDA;
+    int32_t h[8];
+    if (cudaMemcpy(h, ds->scratch, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return BSATTN_ERR_CUDA;
+    if (fallback_units) *fallback_units = h[4];
+    if (fallback_rows) *fallback_rows = h[5];
+    if (device_status)
+        *device_status = (h[0] & bsv::kStatusTimeout) ? BSATTN_ERR_TIMEOUT
+                         : (h[0] & bsv::kStatusIndex) ? BSATTN_ERR_INDEX
+                                                       : BSATTN_OK;
+    return BSATTN_OK;
 }

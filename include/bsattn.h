@@ -17,9 +17,10 @@
  *    serial dependency"; "How is HeyGen optimizing AI video on Google Cloud
  *    TPUs", section "Innovating Beyond Serial Dependencies").  Following the
  *    deep-dive's eligibility check with fallback to online softmax (same
- *    section), rows whose bound is far above any plausible logit take the
- *    running max in the same launch, and rows whose exponentials underflow
- *    anyway are detected and rerun with a running-max (online softmax) kernel.
+ *    section), work units holding a row whose bound is far above any plausible
+ *    logit are sent to a running-max (online softmax) launch of the same kernel
+ *    template, and rows whose exponentials underflow anyway are detected and
+ *    rerun in that launch.
  *
  * Tensors: Q and O are bf16, contiguous [B, H, L, D] with L = nb * block_size;
  * K and V are [B, H, L_kv, D] with L_kv = nb_kv * block_size; 16-byte-aligned
@@ -89,20 +90,20 @@ typedef enum {
 
 /* flags */
 enum {
-    /* bsattn_forward (the default): per query tile and group of 32 rows, the
-       bound softmax when every row of the group is eligible (its bound m_i is at
-       most BSATTN_ELIGIBLE_BOUND), else the online max for that group in the
-       same launch; then the underflow guard on the bound rows and an online-max
-       rerun of the work units holding a flagged row. */
+    /* bsattn_forward (the default): an eligibility check of every work unit (its
+       rows' bounds m_i at most BSATTN_ELIGIBLE_BOUND), the bound softmax over the
+       eligible units with the underflow guard on their rows, then one online-max
+       launch over the other units and the units holding a flagged row. */
     BSATTN_BOUND = 0,
     /* bsattn_forward: run the online-max (running max + rescale) kernel over
        every work unit instead; the A/B baseline of the same kernel. */
     BSATTN_ONLINE_MAX = 1,
-    /* bsattn_forward: skip the rerun of flagged units (testing only: rows
-       whose exponentials underflowed keep an undefined value). */
+    /* bsattn_forward: skip the online-max launch (testing only: rows of units
+       that failed the eligibility check or hold a guard-flagged row keep an
+       undefined value; with N(0,1)-like data there are none). */
     BSATTN_NO_FALLBACK = 2,
-    /* bsattn_forward: the bound softmax for every row whatever its bound (no
-       eligibility switch); the guard and the rerun still apply. */
+    /* bsattn_forward: every unit passes the eligibility check (the bound softmax
+       for every row whatever its bound); the guard and the rerun still apply. */
     BSATTN_BOUND_ONLY = 4,
     /* bsattn_forward, testing only: the first work unit of every CTA never gets
        its query tiles, so the kernel's bounded waits run out (after the layout's
@@ -131,8 +132,8 @@ enum {
     BSATTN_MASK_PER_HEAD = 0x20
 };
 
-/* Eligibility of a row for the bound softmax, in nats: rows with a larger
-   Cauchy-Schwarz bound are computed with the online max in the first launch.
+/* Eligibility of a row for the bound softmax, in nats: a work unit holding a row
+   with a larger Cauchy-Schwarz bound is computed by the online-max launch.
    Every unmasked logit satisfies S_ij >= -m_i, so the denominator of a bound row
    is at least exp(-2 m_i): a row with m_i <= 22 can never trip the guard, and
    above 64 a row passes it only if its best logit lies within 44 nats of a
@@ -160,10 +161,11 @@ enum {
  * an exactly sized MMA with no element mask or padding and none reaches into a
  * masked frame); query tiles of 128 rows that never straddle a frame edge (the
  * last tile of a frame may be partial); and a work list of pairs of query
- * tiles of one frame, sorted by cost, largest first (cost: 100 per key tile
- * for a unit of two query tiles, 83 for one tile, whose softmax cannot overlap
- * another tile's MMAs, plus 150 per unit).  A device layout deals the units to
- * its persistent CTAs (one per SM) by that cost, each to the least-loaded CTA.
+ * tiles of one frame with a cost each (100 per key tile for a unit of two query
+ * tiles, 83 for one tile, whose softmax cannot overlap another tile's MMAs,
+ * plus 150 per unit).  A device layout deals the units to its persistent CTAs
+ * (one per SM) by that cost, each to the least-loaded CTA, in the order that
+ * bsattn_layout_schedule describes.
  * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA, OOM or DEVICE.
  */
 bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,
@@ -200,6 +202,31 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
                                 float *qnorm, float *kmax, float *rowbound, bsattn_stream_t stream);
 
 /*
+ * The same row bounds from per-token norms that the caller's own kernels already
+ * produced, so Q and K are not read again.  The deep-dive (section
+ * 拿掉 softmax 的序列相依) feeds the kernel a small precomputed norm table by
+ * scalar prefetch, and "How is HeyGen optimizing AI video on Google Cloud TPUs"
+ * (section "Innovating Beyond Serial Dependencies") fuses stages through explicit
+ * layout contracts: a QK-norm, RoPE or projection epilogue that writes Q and K
+ * can write their norms beside them, and this call then reads 4 bytes per token
+ * instead of 2 * D.  All pointers are device pointers.
+ *   qnorm     in, fp32 [B, H, L]: |q_i| for each query row.
+ *   knorm     in, fp32 [B, H, L_kv]: |k_j| for each key row.
+ *   scale     the softmax scale; pass the same value to bsattn_forward.
+ *   kmax      out, fp32 [B, H, nb_kv]: the largest knorm of each key block (the
+ *             maximum starts at 0, so negative and NaN entries never win it).
+ *   rowbound  out, fp32 [B, H, L]: (scale * qnorm_i) * max over allowed kb of kmax[kb],
+ *             each product rounded to fp32, exactly as bsattn_row_bounds forms it.
+ * Given the norms bsattn_row_bounds computes, the outputs equal its outputs bit for
+ * bit.  Norms rounded another way also work: the softmax is exact for any shift
+ * that keeps its exponentials in range, and bsattn_forward's guard reruns, with the
+ * online max, every row whose denominator underflowed or overflowed.
+ * Enqueued on `stream`; returns BSATTN_OK, INVALID_ARG or CUDA.
+ */
+bsattn_status bsattn_row_bounds_from_norms(bsattn_layout_t lay, const float *qnorm, const float *knorm, float scale,
+                                           float *kmax, float *rowbound, bsattn_stream_t stream);
+
+/*
  * The attention forward.  All pointers are device pointers.
  *   q         bf16 [B, H, L, D] in; k, v bf16 [B, H, L_kv, D] in.
  *   o         bf16 [B, H, L, D] out (every row is written; rows that read no block get 0).
@@ -212,13 +239,15 @@ bsattn_status bsattn_row_bounds(bsattn_layout_t lay, const void *q, const void *
  *             BSATTN_DEBUG_PLANT_INDEX (the latter only with BSATTN_DEBUG_CHECKS).
  * BSATTN_BOUND computes P = exp(scale * S - m_i) with no running max, rounds P
  * to bf16 for the P.V product and sums the denominator from the same rounded
- * values.  Each warp of the kernel owns 32 rows of a 128-row query tile; when
- * one of them has m_i > BSATTN_ELIGIBLE_BOUND (the deep-dive's eligibility
- * check, section 拿掉 softmax 的序列相依), that warp computes the tile with the
- * running max instead, in the same launch (BSATTN_BOUND_ONLY turns this off).
- * A bound row is flagged when its denominator is below 2^-64 or not finite,
- * and every work unit holding a flagged row is recomputed by the online-max
- * kernel in a second launch on the same stream (no host synchronisation).
+ * values.  Before it, a small kernel checks every work unit (one or two 128-row
+ * query tiles of a frame): a unit holding a row with m_i > BSATTN_ELIGIBLE_BOUND
+ * (the deep-dive's eligibility check, section 拿掉 softmax 的序列相依) is left to
+ * the online-max launch that follows, whole (BSATTN_BOUND_ONLY turns the check
+ * off).  A bound row is flagged when its denominator is below 2^-64 or not
+ * finite, and every work unit holding a flagged row is recomputed by that
+ * online-max launch too, on the same stream (no host synchronisation).  The
+ * launches: a counter clear, the check, the bound kernel and the online-max
+ * kernel; each exits at once when it has nothing to do.
  * Enqueued on `stream`; returns BSATTN_OK, INVALID_ARG or CUDA.
  */
 bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, const void *v, void *o,
@@ -266,28 +295,50 @@ bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q, const void
  * loads the library holds until the process exits.  It calls no allocating CUDA
  * or library routine.
  *   q, k, v, o, scale, rowbound, lse, flags: as for bsattn_forward (device pointers;
- *             rowbound from bsattn_row_bounds or any equal bound).
- *   B, H, L, D, block_size, block_mask: as for bsattn_create_layout (mask on the host; with
- *             BSATTN_MASK_PER_HEAD in flags, one mask per head).
- * Limits: the plan (work units x 24 bytes + the key-tile table, 8 bytes per
- * tile, each part rounded up to 256 bytes) must fit in the array, about 40,000
- * work units (the 720p chunk uses 4,680, the 1080p chunk 9,984); a larger
- * problem returns BSATTN_ERR_UNSUPPORTED before any device work.
+ *             rowbound from bsattn_row_bounds or any equal bound).  flags: BSATTN_BOUND,
+ *             BSATTN_ONLINE_MAX, BSATTN_NO_FALLBACK, BSATTN_BOUND_ONLY, BSATTN_MASK_PER_HEAD
+ *             (one mask per head, as at layout creation) and the testing flag
+ *             BSATTN_DEBUG_STALL.
+ *   B, H, L, D, block_size, block_mask: as for bsattn_create_layout (mask on the host).
+ *             Self-attention only: K and V have L rows per head, like Q (there is no
+ *             streamed-chunk form with L_kv > L; use a layout for that).
+ * The work units are dealt to one persistent CTA per SM by the same cost model as a
+ * device layout, so the kernels run exactly as under bsattn_forward and the output is
+ * bit-identical to it.
+ * Limits: the array holds an 8-int guard header, 28 bytes per schedule slot (16 for
+ * the slot, 4 each for its guard flag, its fallback-list entry and its eligibility;
+ * the slots are the work units dealt to the CTAs, padded with empty slots to a
+ * multiple of the SM count), the key-tile index of 4 * (masks * nb + 1) bytes and
+ * 8 bytes per key tile, each of the four parts rounded up to 256 bytes.  That is
+ * about 37,000 slots (the 720p chunk uses about 4,700, the 1080p chunk about
+ * 10,000); a larger problem returns BSATTN_ERR_UNSUPPORTED before any device work.
  * The first call on a device (with that device current) looks up the array's
- * device address.  Each call copies the plan and zeroed guard counters into the
- * array with one cudaMemcpyAsync from a host buffer that lives only during the
+ * device address.  Each call copies the plan and zeroed guard counters and status into
+ * the array with one cudaMemcpyAsync from a host buffer that lives only during the
  * call, on `stream`, so the call may wait for work already queued on that stream,
  * and it cannot be captured in a CUDA graph: on a capturing stream it returns
- * BSATTN_ERR_UNSUPPORTED before any work (use a layout and bsattn_forward there).  All calls share the array and it keeps the
- * last call's contents: calls whose GPU work overlaps (other streams, other
- * host threads) race.  Statistics are not kept (bsattn_query_stats needs a layout).
- * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA or DEVICE.
+ * BSATTN_ERR_UNSUPPORTED before any work (use a layout and bsattn_forward there).
+ * All calls share the array and it keeps the last call's contents: calls whose GPU
+ * work overlaps (other streams, other host threads) race.  A bounded device wait that
+ * runs out leaves the rows of the units it stopped unwritten; bsattn_noalloc_query
+ * reports it.  Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA or
+ * DEVICE.
  */
 #define BSATTN_NOALLOC_SCRATCH_BYTES (1 << 20)
 bsattn_status bsattn_forward_noalloc(const void *q, const void *k, const void *v, void *o, int32_t B, int32_t H,
                                      int64_t L, int32_t D, int32_t block_size, const uint8_t *block_mask,
                                      float scale, const float *rowbound, float *lse, int32_t flags,
                                      bsattn_stream_t stream);
+
+/*
+ * Statistics of the last bsattn_forward_noalloc on the current device, read from its
+ * static array without allocating: synchronises `stream`, then copies the guard
+ * header with cudaMemcpy.  Outputs as for bsattn_query_stats (each nullable), but for
+ * the last call only: every call clears the header, device status included.  Returns
+ * BSATTN_OK, CUDA or DEVICE.
+ */
+bsattn_status bsattn_noalloc_query(int64_t *fallback_rows, int64_t *fallback_units, int32_t *device_status,
+                                   bsattn_stream_t stream);
 
 /* Free the layout's device buffers and host plan.  NULL is ignored. */
 void bsattn_destroy(bsattn_layout_t lay);
@@ -308,6 +359,19 @@ const char *bsattn_status_string(bsattn_status st);
  */
 bsattn_status bsattn_query_stats(bsattn_layout_t lay, int64_t *fallback_rows, int64_t *fallback_units,
                                  int32_t *device_status, bsattn_stream_t stream);
+
+/*
+ * The eligibility check of the last bsattn_forward on this layout (the deep-dive's
+ * per-head check, section 拿掉 softmax 的序列相依, made per work unit).  Synchronises
+ * `stream`.
+ *   bound_units   work units whose rows all had m_i <= BSATTN_ELIGIBLE_BOUND, computed
+ *                 by the bound softmax (nullable).
+ *   online_units  work units sent to the online-max launch (nullable).
+ * Both 0 after a BSATTN_ONLINE_MAX forward, which checks nothing.  For
+ * bsattn_forward_host, summed over the call's chunks.
+ */
+bsattn_status bsattn_query_eligibility(bsattn_layout_t lay, int64_t *bound_units, int64_t *online_units,
+                                       bsattn_stream_t stream);
 
 /* Plan summary of a layout (host only). */
 typedef struct {
@@ -333,12 +397,28 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
  *   row_ptr  int32 [mask_heads * nb + 1], col_idx int32 [nnz_blocks]: allowed key blocks of
  *            segment s in col_idx[row_ptr[s] .. row_ptr[s+1]), ascending;
  *   units    int32 [n_units * 4]: (b * H + h, query block, first query tile, tiles in the unit (1 or 2)),
- *            in execution order;
+ *            in (b * H + h, query block, first query tile) order;
  *   tile_ptr int32 [mask_heads * nb + 1], tiles int32 [key_tiles * 2]: the key tiles of segment s are
  *            (tiles[2t], tiles[2t+1]) = (first key within the head, width) for t in [tile_ptr[s], tile_ptr[s+1]).
  */
 bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units,
                                    int32_t *tile_ptr, int32_t *tiles);
+
+/*
+ * The schedule a device layout runs for `grid` persistent CTAs (host only; a device
+ * layout uses grid = the SM count, or fewer CTAs when it has fewer units).  The units
+ * are taken in plan order, (head, frame, tile), so that the CTAs running at any one time
+ * work on one or two heads and read each K/V tile from DRAM about once; the last
+ * 4 * grid units (all of them, when there are fewer) are taken by cost instead, largest
+ * first.  Each unit goes to the least-loaded CTA by the cost model of
+ * bsattn_create_layout.  Slot k * grid + c holds CTA c's k-th unit as 4 int32 in the
+ * format of `units` above; empty slots are (0, 0, 0, 0).
+ *   grid     >= 1.
+ *   slots    host int32 [*n_slots * 4] out, or NULL to learn the size.
+ *   n_slots  out: slots, a multiple of grid.
+ * Returns BSATTN_OK, INVALID_ARG or OOM.
+ */
+bsattn_status bsattn_layout_schedule(bsattn_layout_t lay, int32_t grid, int32_t *slots, int32_t *n_slots);
 
 #ifdef __cplusplus
 }

@@ -53,9 +53,10 @@ def run_gpu(ba, q, k, v, mask, bs, scale, flags=0, want_meta=True, lay=None):
     ba.bsattn_row_bounds(lay, dq, dk, scale, qn, km, rb)
     ba.bsattn_forward(lay, dq, dk, dv, o, scale, rb, lse, flags)
     rows, units, status = ba.bsattn_query_stats(lay)
+    bound_units, online_units = ba.bsattn_query_eligibility(lay)
     torch.cuda.synchronize()
     out = dict(o=_host_bf16(o).reshape(-1, D), lse=lse.cpu().numpy().reshape(-1), fb_rows=rows, fb_units=units,
-               status=status, o_raw=o)
+               status=status, o_raw=o, bound_units=bound_units, online_units=online_units)
     if want_meta:
         out.update(qnorm=qn.cpu().numpy(), kmax=km.cpu().numpy(), rowbound=rb.cpu().numpy())
     if own:
@@ -231,10 +232,10 @@ def _scaled_key(w, factor):
 
 
 def _predicted_flags(q, k, v, mask, bs, scale, eligible=np.inf):
-    """(must, may) counts of guard-flagged rows: a row is a bound row when every valid row of its
-    32-row group (same head, frame, 128-row query tile and 32-row quarter) has a bound <= eligible;
-    a bound row must be flagged when ln l < ln 2^-65 and may be when ln l < ln 2^-63, l being the
-    bound-shifted denominator."""
+    """(must, may) counts of guard-flagged rows: a row is a bound row when every row of its work
+    unit (same head and frame, query tiles 2c and 2c + 1, i.e. frame rows 256c .. 256c + 255) has
+    a bound <= eligible; a bound row must be flagged when ln l < ln 2^-65 and may be when
+    ln l < ln 2^-63, l being the bound-shifted denominator."""
     B, H, L, D = q.shape
     _, lse, _ = oracle.attention(q, k, v, mask, bs, scale)
     _, _, m32 = oracle.metadata_f32(q, k, mask, bs, scale)
@@ -242,8 +243,8 @@ def _predicted_flags(q, k, v, mask, bs, scale, eligible=np.inf):
     log_l = lse - m
     r = np.arange(B * H * L)
     pos = r % L
-    qt_per_block = (bs + 127) // 128
-    group = ((r // L) * (L // bs) + pos // bs) * (4 * qt_per_block) + (pos % bs) // 32
+    units_per_block = (bs + 255) // 256
+    group = ((r // L) * (L // bs) + pos // bs) * units_per_block + (pos % bs) // 256
     online = np.zeros(B * H * L, dtype=bool)
     for g in np.unique(group):
         sel = group == g
@@ -277,16 +278,22 @@ def test_guard_forced_and_zero_queries(ba):
     check_o(res2["o"][ok_rows], O[ok_rows], "guard, unflagged rows")
 
 
-def test_eligibility_switch_takes_loose_rows_online_in_one_launch(ba):
-    # Default mode on the same inputs: the rows whose bound is above the eligibility limit are
-    # computed with the running max in the first launch, so nothing is flagged or rerun.
+def test_eligibility_check_sends_loose_units_online(ba):
+    # Default mode on the same inputs: the work units holding a row whose bound is above the
+    # eligibility limit go to the online-max launch, whole, before any bound softmax runs, so the
+    # guard flags nothing; the check's counts are exactly the units the oracle's bounds predict.
     w = synth.WORKLOADS["tiny"]
     q, k, v = _scaled_key(w, 1e4)
     mask, bs, scale = w.block_mask(), w.block, w.scale
     must, may, _, online = _predicted_flags(q, k, v, mask, bs, scale, eligible=64.0)
     assert online.any() and must == may == 0
-    res = full_case(ba, q, k, v, mask, bs, scale, flags=0, what="eligibility switch")
+    res = full_case(ba, q, k, v, mask, bs, scale, flags=0, what="eligibility check")
     assert res["fb_rows"] == 0 and res["fb_units"] == 0
+    n_units = w.B * w.H * w.nb * ((bs + 255) // 256)
+    r = np.arange(w.B * w.H * w.L)
+    unit_of_row = ((r // w.L) * w.nb + (r % w.L) // bs) * ((bs + 255) // 256) + (r % bs) // 256
+    want_online = len(np.unique(unit_of_row[online]))
+    assert res["online_units"] == want_online and res["bound_units"] == n_units - want_online
 
 
 def test_guard_fires_on_eligible_rows(ba):
@@ -352,8 +359,12 @@ def test_workload_sampled(ba, name, heads):
     check_o(res["o"][rows], O, name)
     assert np.max(np.abs(res["lse"][rows] - lse)) <= LSE_MAX
     assert np.all(np.isfinite(res["o"]))
-    assert res["fb_rows"] == 0  # stress: loose rows take the running max in the first launch
+    assert res["fb_rows"] == 0  # stress: loose units go to the online launch before any bound softmax
     assert res["status"] == 0
+    if name != "stress":
+        assert res["online_units"] == 0  # N(0,1) data: every unit is eligible
+    else:
+        assert res["online_units"] > 0
     if name == "stress":
         # the bound path for every row: the guard flags the loose rows and the rerun fixes them
         res2 = run_gpu(ba, q, k, v, mask, w.block, w.scale, flags=4, want_meta=False)
@@ -511,4 +522,74 @@ def test_cuda_graph_capture_and_replay(ba):
         check_o(_host_bf16(replayed).reshape(-1, w.D), O, f"graph replay seed {seed}")
     _, _, status = ba.bsattn_query_stats(lay)
     assert status == 0
+    lay.destroy()
+
+
+# ------------------------------------------------------------------------------------------------
+# row bounds from norms supplied by the caller's producer kernel
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "stream_small", "small_heads"])
+def test_row_bounds_from_norms_bit_exact(ba, name):
+    # The norm table of the deep-dive (section 拿掉 softmax 的序列相依) handed in by a
+    # producer: given the oracle's own per-token norms, kmax and rowbound are the oracle's
+    # bit for bit, and the forward with that bound equals the forward after
+    # bsattn_row_bounds bit for bit.  Arbitrary positive norms (not the norms of Q and K)
+    # are checked against the oracle's block maximum and row bound as well.
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.make_qkv(w)
+    mask = w.block_mask()
+    B, H, L, D = q.shape
+    L_kv = k.shape[2]
+    nbkv = L_kv // w.block
+    lay = ba.bsattn_create_layout(B, H, L, D, w.block, mask, L_kv=L_kv)
+    qn_o, km_o, rb_o = oracle.metadata_f32(q, k, mask, w.block, w.scale)
+    kn_o = oracle.row_norms_f32(k)
+    dqn = torch.from_numpy(qn_o).cuda()
+    dkn = torch.from_numpy(kn_o).cuda()
+    km = torch.full((B, H, nbkv), float("nan"), dtype=torch.float32, device="cuda")
+    rb = torch.full((B, H, L), float("nan"), dtype=torch.float32, device="cuda")
+    ba.bsattn_row_bounds_from_norms(lay, dqn, dkn, w.scale, km, rb)
+    torch.cuda.synchronize()
+    assert np.array_equal(km.cpu().numpy().view(np.uint32), km_o.view(np.uint32))
+    assert np.array_equal(rb.cpu().numpy().view(np.uint32), rb_o.view(np.uint32))
+
+    res = run_gpu(ba, q, k, v, mask, w.block, w.scale, lay=lay)
+    dq, dk, dv = _dev(q), _dev(k), _dev(v)
+    o = torch.full_like(dq, float("nan"))
+    ba.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), res["o_raw"].view(torch.int16))
+
+    rng = np.random.default_rng(3)
+    qn_r = (rng.random((B, H, L)) * 20).astype(np.float32)
+    kn_r = (rng.random((B, H, L_kv)) * 20).astype(np.float32)
+    kn_r[0, 0, : w.block] = 0.0  # a key block whose norms are all zero
+    km_want = oracle.block_max_f32(kn_r, w.block)
+    rb_want = oracle.row_bounds_f32(qn_r, km_want, mask, w.block, w.scale)
+    ba.bsattn_row_bounds_from_norms(lay, torch.from_numpy(qn_r).cuda(), torch.from_numpy(kn_r).cuda(), w.scale,
+                                    km, rb)
+    torch.cuda.synchronize()
+    assert np.array_equal(km.cpu().numpy().view(np.uint32), km_want.view(np.uint32))
+    assert np.array_equal(rb.cpu().numpy().view(np.uint32), rb_want.view(np.uint32))
+    lay.destroy()
+
+
+def test_row_bounds_from_norms_720p(ba):
+    # full size: the bound from the oracle's norms equals bsattn_row_bounds' bit for bit
+    w = synth.WORKLOADS["720p"]
+    q, k, v = synth.make_qkv(w)
+    B, H, L, D = q.shape
+    lay = ba.bsattn_create_layout(B, H, L, D, w.block, w.block_mask())
+    dq, dk = _dev(q), _dev(k)
+    qn = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    km = torch.empty((B, H, w.nb), dtype=torch.float32, device="cuda")
+    rb = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    ba.bsattn_row_bounds(lay, dq, dk, w.scale, qn, km, rb)
+    dkn = torch.from_numpy(oracle.row_norms_f32(k)).cuda()
+    km2, rb2 = torch.empty_like(km), torch.empty_like(rb)
+    ba.bsattn_row_bounds_from_norms(lay, qn, dkn, w.scale, km2, rb2)
+    torch.cuda.synchronize()
+    assert torch.equal(km.view(torch.int32), km2.view(torch.int32))
+    assert torch.equal(rb.view(torch.int32), rb2.view(torch.int32))
     lay.destroy()

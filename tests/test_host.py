@@ -81,12 +81,57 @@ def test_plan_matches_oracle(lib, name):
         assert nt in (1, 2) and qt0 % 2 == 0 and qt0 + nt <= nqt
         seen[bh, qb, qt0:qt0 + nt] += 1
     assert np.all(seen == 1)
-    # largest cost first, by the documented model: 100 per key tile for a unit of two query
-    # tiles, 83 for one tile, plus 150 per unit
-    segment = (units[:, 0] % w.H if len(masks) > 1 else 0) * w.nb + units[:, 1]
+    # plan order: (head, frame, first query tile)
+    key = (units[:, 0].astype(np.int64) * w.nb + units[:, 1]) * nqt + units[:, 2]
+    assert np.all(np.diff(key) > 0)
+    lay.destroy()
+
+
+def _unit_cost(units, tile_ptr, H, nb, per_head):
+    # the documented model: 100 per key tile for a unit of two query tiles, 83 for one, plus 150
+    segment = (units[:, 0] % H if per_head else 0) * nb + units[:, 1]
     ntile = np.diff(tile_ptr)[segment]
-    cost = ntile * np.where(units[:, 3] == 2, 100, 83) + 150
-    assert np.all(np.diff(cost) <= 0)
+    return ntile * np.where(units[:, 3] == 2, 100, 83) + 150
+
+
+@pytest.mark.parametrize("name,grid", [("720p", 148), ("stream", 148), ("small", 148), ("small", 7),
+                                       ("720p_heads", 148), ("1080p", 148), ("tiny", 148)])
+def test_schedule_deals_every_unit_once_head_major_then_by_cost(lib, name, grid):
+    w = synth.WORKLOADS[name]
+    mask = w.block_mask()
+    lay = bsattn.bsattn_create_layout(w.B, w.H, w.L, w.D, w.block, mask, bsattn.BSATTN_PLAN_ONLY, L_kv=w.L_kv)
+    _, _, units, tile_ptr, _ = bsattn.bsattn_layout_export(lay, with_tiles=True)
+    n = len(units)
+    g = min(grid, n)
+    slots = bsattn.bsattn_layout_schedule(lay, g)
+    assert len(slots) % g == 0
+    real = slots[:, 3] > 0
+    assert np.all(slots[~real] == 0)
+    # every unit exactly once
+    got = sorted(map(tuple, slots[real]))
+    assert got == sorted(map(tuple, units))
+    # the order the units were dealt in: plan order, then the last 4 * grid units by cost
+    cost_of = {tuple(u): c for u, c in zip(units, _unit_cost(units, tile_ptr, w.H, w.nb, mask.ndim == 3))}
+    n_tail = min(n, 4 * g)
+    head = [tuple(u) for u in units[:n - n_tail]]
+    tail = sorted((tuple(u) for u in units[n - n_tail:]), key=lambda u: -cost_of[u])  # stable
+    # replay the least-loaded deal (ties: lowest CTA) and compare slot by slot
+    import heapq
+    heap = [(0, c) for c in range(g)]
+    per = [[] for _ in range(g)]
+    for u in head + tail:
+        load, c = heapq.heappop(heap)
+        per[c].append(u)
+        heapq.heappush(heap, (load + cost_of[u], c))
+    K = max(len(x) for x in per)
+    assert len(slots) == K * g
+    for kk in range(K):
+        for c in range(g):
+            want = per[c][kk] if kk < len(per[c]) else (0, 0, 0, 0)
+            assert tuple(slots[kk * g + c]) == want
+    # balance: the most loaded CTA is within one unit of the mean load
+    loads = [sum(cost_of[u] for u in x) for x in per]
+    assert max(loads) <= sum(loads) / g + max(cost_of.values())
     lay.destroy()
 
 
