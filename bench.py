@@ -48,9 +48,11 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples taken during the timed region."""
+    """nvidia-smi clock / throttle-reason samples, with their host timestamps, taken from the
+    warm-up to the end of the last measured region, so that each region's clocks can be
+    binned (``region``)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -72,30 +74,42 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        """End sampling; returns the parsed samples (time, sm MHz, max MHz, power W, reasons)."""
+        self.samples = []
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+            return self.samples
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], None, set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax = float(parts[2]), float(parts[3])
+                pw = float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None
             except ValueError:
                 continue
-            for n, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            reasons = {n for n, val in zip(names, parts[6:10]) if val.lower() == "active"}
+            self.samples.append((ts, sm, smax, pw, reasons))
+        return self.samples
+
+    def region(self, t0: float, t1: float) -> dict:
+        """Median SM clock, max clock, median power and the throttle reasons seen in [t0, t1]."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sel = [x for x in self.samples if t0 <= x[0] <= t1]
+        pw = [x[3] for x in sel if x[3] is not None]
+        return {"sm_mhz": statistics.median(x[1] for x in sel) if sel else None,
+                "sm_max_mhz": max((x[2] for x in sel), default=None),
+                "power_w": statistics.median(pw) if pw else None,
+                "reasons": sorted(set().union(*(x[4] for x in sel))) if sel else [], "samples": len(sel)}
 
 
 def rank_workload(w, rank: int):
@@ -254,7 +268,7 @@ def main():
             step()
         torch.cuda.synchronize()
         lay.destroy()
-        print(json.dumps({"profile_run": w.name, "steps": args.warmup + args.steps, "kernels_per_step": 4}))
+        print(json.dumps({"profile_run": w.name, "steps": args.warmup + args.steps, "kernels_per_step": 5}))
         return
 
     # ---- warm-up: W steps, continued until the clock sampler (started now) is running under load
@@ -266,6 +280,9 @@ def main():
         torch.cuda.synchronize()
         n_warm += 1
     fb_rows, fb_units, dev_status = bsattn.bsattn_query_stats(lay, stream)
+    bound_units, online_units = bsattn.bsattn_query_eligibility(lay, stream)
+    for _ in range(3):  # back under load after the queries' synchronisation
+        step()
 
     # ---- main timed region: K steps, barrier + synchronize on both sides, clocks sampled meanwhile
     if world > 1:
@@ -274,30 +291,50 @@ def main():
     # events at each step boundary and between the bounds and the forward call (the
     # per-stage split and the attention launch time come from the timed region itself)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    t_main0 = time.time()
     evs[0].record(stream)
     for i in range(args.steps):
         step(evs[2 * i + 1])
         evs[2 * i + 2].record(stream)
     torch.cuda.synchronize()
+    t_main1 = time.time()
     if world > 1:
         dist.barrier()
     ms_total = evs[0].elapsed_time(evs[-1])
     bounds_live = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)]
     fwd_live = [evs[2 * i + 1].elapsed_time(evs[2 * i + 2]) for i in range(args.steps)]
-    clk = clocks.stop()
     ms_total = max_over_ranks(ms_total, world, "cuda")
     ms_step = ms_total / args.steps
     value = job_throughput(flop_step, world, ms_step)
 
-    # ---- A/B: the same forward with the online-max kernel everywhere, and with the bound kernel
-    # alone (no rerun launch), timed back to back on the same inputs
-    attn_ms = timed(lambda: bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None,
-                                                  bsattn.BSATTN_NO_FALLBACK, stream), max(args.steps, 5))
-    online_ms = timed(lambda: bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None,
-                                                    bsattn.BSATTN_ONLINE_MAX, stream), max(args.steps, 5))
+    # ---- A/B under the same sustained load: the default forward (eligibility check, bound
+    # kernel, online launch over the rest) and the online-max kernel over every unit on the same
+    # inputs, in alternating blocks of about 0.3 s each, straight after the timed region, with
+    # the clocks of each block binned.  The default forward's blocks (back to back, without the
+    # bounds kernel in between) also give the forward-alone time to set against the forward
+    # inside the timed steps.
+    n_blk = max(5, int(0.3 / max(ms_step * 1e-3, 1e-4)))
+    ab_ms = {"bound": [], "online": []}
+    ab_win = {"bound": [], "online": []}
+    for _ in range(2):
+        for mode, fl in (("bound", bsattn.BSATTN_BOUND), ("online", bsattn.BSATTN_ONLINE_MAX)):
+            t0 = time.time()
+            ab_ms[mode] += timed(lambda: bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None, fl, stream),
+                                 n_blk)
+            ab_win[mode].append((t0, time.time()))
     bounds_ms = timed(lambda: bsattn.bsattn_row_bounds(lay, dq, dk, w.scale, qn, km, rb, stream),
                       max(args.steps, 5))
-    attn_avg = float(np.mean(attn_ms))
+    clocks.stop()
+    clk = clocks.region(t_main0, t_main1)
+
+    def region_mhz(wins):
+        vals = [clocks.region(a, b)["sm_mhz"] for a, b in wins]
+        vals = [x for x in vals if x is not None]
+        return float(np.mean(vals)) if vals else None
+
+    bound_avg = float(np.mean(ab_ms["bound"]))
+    online_avg = float(np.mean(ab_ms["online"]))
+    bound_mhz, online_mhz = region_mhz(ab_win["bound"]), region_mhz(ab_win["online"])
     fwd_avg = float(np.mean(fwd_live))
     peaks, peak_src = _peaks()
     # the forward call inside the timed region: workspace memset, the bound-softmax kernel and the
@@ -329,7 +366,7 @@ def main():
     e2e_ms = timed(e2e_step, max(3, args.steps // 4))
     e2e_val = job_throughput(flop_step, world, max_over_ranks(float(np.mean(e2e_ms)), world, "cuda"))
 
-    launches_per_step = 4  # norms, rowbound, bound attention, rerun of flagged units (timed region)
+    launches_per_step = 5  # norms, rowbound, eligibility route, bound attention, online launch (timed region)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
@@ -342,10 +379,21 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "stages_ms": {"row_bounds": float(np.mean(bounds_live)), "forward": fwd_avg},
-            "ab": {"bound_attn_ms": attn_avg, "online_max_attn_ms": float(np.mean(online_ms)),
-                   "bound_speedup_vs_online": float(np.mean(online_ms)) / attn_avg,
+            "ab": {"how": f"alternating blocks of {n_blk} forward calls back to back, 2 per mode, after the "
+                          "timed region; clocks binned per block",
+                   "bound_fwd_ms": bound_avg, "bound_sm_mhz": bound_mhz,
+                   "online_max_fwd_ms": online_avg, "online_sm_mhz": online_mhz,
+                   "bound_speedup_vs_online": online_avg / bound_avg,
+                   "bound_speedup_at_equal_clock": ((online_avg * online_mhz) / (bound_avg * bound_mhz)
+                                                    if bound_mhz and online_mhz else None),
                    "row_bounds_ms": float(np.mean(bounds_ms))},
+            "forward_in_step_vs_alone": {
+                "in_step_ms": fwd_avg, "in_step_sm_mhz": clk.get("sm_mhz"),
+                "alone_ms": bound_avg, "alone_sm_mhz": bound_mhz,
+                "in_step_ms_x_mhz": fwd_avg * clk["sm_mhz"] if clk.get("sm_mhz") else None,
+                "alone_ms_x_mhz": bound_avg * bound_mhz if bound_mhz else None},
             "guard": {"fallback_rows": fb_rows, "fallback_units": fb_units, "device_status": dev_status},
+            "eligibility": {"bound_units": bound_units, "online_units": online_units},
             "wasted_mma_rows_pct": 100.0 * (lay.info.mma_rows - B * H * L) / lay.info.mma_rows}
 
     if rank == 0 and not args.no_cpu_baseline:
