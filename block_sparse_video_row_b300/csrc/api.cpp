@@ -290,6 +290,18 @@ int32_t schedule_units(const bsattn_layout_s &lay, int32_t G, std::vector<int32_
     return static_cast<int32_t>(K * G);
 }
 
+bool encode_o_store_map(CUtensorMap *m, const AttnParams &p, int D) {
+    if (!encode_fn()) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.block),
+                                static_cast<cuuint64_t>(p.bh) * static_cast<cuuint64_t>(p.nb)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(D) * 2 * p.block};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.o, dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_layout_maps(const bsattn_layout_s *lay, const void *q, const void *k, const void *v, CUtensorMap *tq,
                         CUtensorMap *tk, CUtensorMap *tv) {
     return encode_fn() && encode_q_map(tq, *lay, q) && encode_kv_map(tk, *lay, k) && encode_kv_map(tv, *lay, v);

@@ -29,7 +29,10 @@
 //   warps 4-11  softmax and epilogue.  Warp w reads TMEM lanes 32*(w%4).. (its
 //               rows) and column half h = (w-4)/4 of the key tile, so all eight
 //               warps work on one query tile at a time: tile 0's softmax runs
-//               while the tensor cores run tile 1's MMAs, and vice versa.
+//               while the tensor cores run tile 1's MMAs, and vice versa.  In
+//               the epilogue each warp stages its 32 rows x 32 columns of O in
+//               shared memory and one lane stores them with a TMA tensor store,
+//               clipped at the frame edge by the Q/O frame layout.
 // TMEM (512 columns): S_0/P_0 at column 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
 // P (bf16, two per 32-bit column) of key half h overwrites the first 32 of that
 // half's 64 S columns: keys 64h + 2c, 64h + 2c + 1 sit in column 64h + c.
@@ -65,7 +68,8 @@ struct AttnCfg {
     static constexpr int SMEM_CAP = 232448;           // 227 KB per CTA
     static constexpr int BAR_BYTES = 512;             // mbarriers, TMEM slot, abort flag
     static constexpr int XCHG_BYTES = 2 * 2 * kQTile * 4;  // row exchange: [parity][half][row] fp32
-    static constexpr int RESERVED = 1024 + BAR_BYTES + XCHG_BYTES;  // + alignment slack
+    static constexpr int OST_BYTES = 8 * 2048;                       // O staging: 2 KB per softmax warp
+    static constexpr int RESERVED = 1024 + BAR_BYTES + XCHG_BYTES + 1024 + OST_BYTES;  // + alignment slack
     static constexpr int STAGES_FIT = (SMEM_CAP - RESERVED - 2 * Q_TILE) / (2 * KV_TILE);
     static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
     static_assert(STAGES >= 2, "shared memory");
@@ -74,7 +78,8 @@ struct AttnCfg {
     static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
     static constexpr int OFF_XCHG = OFF_BAR + BAR_BYTES;
-    static constexpr int SMEM_USED = OFF_XCHG + XCHG_BYTES + 1024;
+    static constexpr int OFF_OST = (OFF_XCHG + XCHG_BYTES + 1023) / 1024 * 1024;
+    static constexpr int SMEM_USED = OFF_OST + OST_BYTES + 1024;
     // Above half of the SM's shared memory, so one CTA (and one TMEM owner) per SM.
     static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static_assert(SMEM <= SMEM_CAP, "shared memory");
@@ -355,7 +360,8 @@ __device__ __forceinline__ bool pair_exchange(const Bars &bar, int q, int h, int
 template <int D, bool ONLINE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const AttnParams p) {
     using C = AttnCfg<D>;
     // Positions of this launch: the bound launch walks the schedule unless the route kernel
     // sent every unit online; the fallback launch walks the schedule when it sent some
@@ -606,6 +612,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t tO1 = tmem + lane_base + C::COL_O1 + DC * h;
         const float c1 = p.scale_log2;
         const uint64_t c1x2 = f2_make(c1, c1);
+        uint8_t *ost = smem + C::OFF_OST + (warp - 4) * 2048;  // this warp's O staging (32 rows x 64 B)
+        bool ost_busy = false;
         uint32_t s_uses0 = 0, s_uses1 = 0, o_uses0 = 0, o_uses1 = 0, x_uses = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_seq && ok; i += gridDim.x) {
@@ -723,8 +731,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint64_t inv2 = f2_make(inv, inv);
                 const bool valid = t ? valid1 : valid0;
                 const int64_t grow = row0 + t * kQTile;
-                uint16_t *orow = p.o + grow * D + DC * h;
                 const uint32_t tO = t ? tO1 : tO0;
+                // O rows of this warp go out as 32-row boxes of a 3-D (D, frame rows, frames) map:
+                // a box running past the frame's last row is clipped there, one starting past it
+                // is not issued.  y0: the box's first row in the frame.
+                const int y0 = (U.z + t) * kQTile + q * 32;
 #pragma unroll
                 for (int c = 0; c < DC / 32; ++c) {
                     uint32_t a[32];
@@ -738,13 +749,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         f2_split(f2_mul(f2_from_bits(a[2 * e], a[2 * e + 1]), inv2), x0, x1);
                         wv[e] = pack_bf16x2(x0, x1);
                     }
-                    if (valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                        dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-                        dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
-                        dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+                    if (ost_busy) {  // the previous store must have read the staging buffer
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
                     }
+                    // row = lane, 64 B per row, 16-byte chunk k at (k ^ ((row >> 1) & 3)) (64-byte swizzle)
+                    uint8_t *rowp = ost + lane * 64;
+                    const int sw = (lane >> 1) & 3;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4 *>(rowp + ((k ^ sw) << 4)) =
+                            make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && y0 < p.block) {
+                        tma_store_3d(&tm_o, DC * h + 32 * c, y0, U.x * p.nb + U.y, ost);
+                        bulk_commit();
+                    }
+                    ost_busy = true;
                 }
                 if (h == 0) {
                     const float mrow = t ? mrow1 : mrow0;
@@ -773,6 +795,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
         }
+        if (lane == 0) bulk_wait0();  // the last stores are complete (and their staging read)
+        __syncwarp();
         tc_fence_before();
         cta_barrier();
     }
@@ -781,7 +805,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D, bool ONLINE>
 cudaError_t launch_fwd_instance(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const AttnParams &p, int n_ctas, cudaStream_t s) {
-    bsattn_fwd_kernel<D, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D>::SMEM, s>>>(tq, tk, tv, p);
+    CUtensorMap to;
+    if (!encode_o_store_map(&to, p, D)) return cudaErrorInvalidValue;
+    bsattn_fwd_kernel<D, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D>::SMEM, s>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 

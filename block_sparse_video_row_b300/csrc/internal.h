@@ -101,6 +101,11 @@ __host__ __device__ __forceinline__ int plan_segment(int mask_heads, int heads, 
     return (mask_heads > 1 ? static_cast<int>(bh % heads) * nb : 0) + qb;
 }
 
+// TMA map for the epilogue's O stores (built per launch from p.o): 3-D (D, block rows,
+// B*H*nb frames), box 32 columns x 32 rows, 64-byte swizzle.  False if the driver entry
+// point is missing or the driver rejects the map.
+bool encode_o_store_map(CUtensorMap *m, const AttnParams &p, int D);
+
 // Launchers (return the launch error, if any).
 // The eligibility check of every schedule slot before the forward's two launches: a
 // unit with a row bound above p.elig_m is routed to the online-max launch; also

@@ -296,6 +296,23 @@ def test_eligibility_check_sends_loose_units_online(ba):
     assert res["online_units"] == want_online and res["bound_units"] == n_units - want_online
 
 
+def test_eligibility_check_on_a_streamed_chunk_with_per_head_masks(ba):
+    # One key of head 1 (rule 1: window +-2) in frame 5 made 1e4 times longer: every query
+    # frame of the chunk (5, 6, 7) reads frame 5 under head 1's mask, so all of head 1's units
+    # fail the check and no other unit does; the whole chunk still matches the oracle.
+    w = synth.WORKLOADS["stream_heads"]
+    q, k, v = synth.make_qkv(w)
+    k = k.copy()
+    k[0, 1, 5 * w.block + 100] = synth.f32_to_bf16_bits(
+        (synth.bf16_bits_to_f64(k[0, 1, 5 * w.block + 100]) * 1e4).astype(np.float32))
+    mask = w.block_mask()
+    res = full_case(ba, q, k, v, mask, w.block, w.scale, what="streamed per-head eligibility")
+    units_per_frame = (w.block + 255) // 256
+    assert res["online_units"] == w.nq * units_per_frame
+    assert res["bound_units"] == (w.B * w.H - 1) * w.nq * units_per_frame
+    assert res["fb_rows"] == 0
+
+
 def test_guard_fires_on_eligible_rows(ba):
     # A key 5x longer puts the bounds of the rows that read it between 22 and 64 nats (57 at most):
     # they stay on the bound path (eligible), and those whose best logit lies > 44 nats below the
@@ -593,3 +610,27 @@ def test_row_bounds_from_norms_720p(ba):
     assert torch.equal(km.view(torch.int32), km2.view(torch.int32))
     assert torch.equal(rb.view(torch.int32), rb2.view(torch.int32))
     lay.destroy()
+
+
+def test_ulysses_head_groups_on_one_gpu_equal_the_whole_attention(ba, monkeypatch):
+    # The head-group pipeline of ulysses.py with one rank (NCCL, the exchanges are copies):
+    # each group's attention runs through the C ABI on its heads' slice of the per-head masks,
+    # and the result equals one forward over all heads bit for bit (every unit computes the
+    # same rows in the same order, whatever the grid and schedule).
+    import torch.distributed as dist
+    from block_sparse_video_row_b300 import ulysses
+    monkeypatch.setenv("NCCL_NVLS_ENABLE", "0")
+    monkeypatch.setenv("MASTER_ADDR", "127.0.0.1")
+    monkeypatch.setenv("MASTER_PORT", "29637")
+    w = synth.WORKLOADS["small_heads"]
+    q, k, v = synth.make_qkv(w)
+    dq, dk, dv = _dev(q), _dev(k), _dev(v)
+    mask = w.block_mask()
+    whole = ba.attention(dq, dk, dv, mask, w.block, w.scale)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        got = ulysses.ulysses_attention(dq, dk, dv, ulysses.bsattn_group_attend(mask, w.block, w.scale), groups=4)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert torch.equal(got.view(torch.int16), whole.view(torch.int16))

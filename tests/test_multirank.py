@@ -43,7 +43,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_shard_and_reduce():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
         res = dict(out)

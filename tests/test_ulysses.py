@@ -81,7 +81,7 @@ def test_ulysses_two_ranks_equal_the_unsharded_attention(per_head, groups):
     import oracle
     from block_sparse_video_row_b300 import synth
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), per_head, groups, out), nprocs=world,
                            start_method="spawn")
