@@ -175,8 +175,10 @@ extern "C" bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q,
         return BSATTN_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
     const int32_t BH = lay->B * lay->H;
-    // About eight chunks: enough to overlap copies with kernels, each still a full grid.
-    const int32_t G = pairs_per_chunk > 0 ? std::min(pairs_per_chunk, BH) : std::max(1, (BH + 7) / 8);
+    // About twelve chunks: the copies of one chunk overlap the kernels of its neighbours,
+    // and the first copy-in and last copy-out, which nothing overlaps, stay short (at 720p,
+    // two pairs per chunk measured 1.3% faster than three and 3.4% faster than six).
+    const int32_t G = pairs_per_chunk > 0 ? std::min(pairs_per_chunk, BH) : std::max(1, (BH + 11) / 12);
     if (lay->host && lay->host->G != G) {
         bsv::host_pipe_destroy(lay->host);
         lay->host = nullptr;

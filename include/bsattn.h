@@ -263,7 +263,7 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
  *   scale, flags  as for bsattn_forward (BSATTN_ONLINE_MAX skips the row bounds;
  *             the testing flags are refused).
  *   lse       optional host fp32 [B, H, L] out, as for bsattn_forward.
- *   pairs_per_chunk  (batch, head) pairs per pipeline chunk; 0 picks about eight
+ *   pairs_per_chunk  (batch, head) pairs per pipeline chunk; 0 picks about twelve
  *             chunks.
  * The (batch, head) pairs are processed in chunks: copy-in, kernels and copy-out
  * run on three streams owned by the layout, with two sets of device staging
