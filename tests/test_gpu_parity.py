@@ -209,6 +209,43 @@ def test_random_shapes(ba, seed):
     full_case(ba, q, k, v, mask, bs, scale, what=f"random {seed}: D{D} {B}x{H} {nq}/{nkv}x{bs} mask{shape}")
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_loose_keys_route_and_guard(ba, seed):
+    # Random small problems as above, with a few keys made 10^0.5 .. 10^4 times longer, so
+    # that some units fail the eligibility check (routed online), some bound rows underflow
+    # (flagged and rerun) and the rest stay on the bound path.  Every row against the
+    # oracle; the online-unit count exactly as the oracle's fp32 bounds predict (any row of
+    # the unit above 64 nats); the flagged rows inside the guard's must/may band.
+    rng = np.random.default_rng(3000 + seed)
+    D = int(rng.choice([64, 128]))
+    B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+    bs = 16 * int(rng.integers(1, 26))
+    nkv = int(rng.integers(1, 6))
+    nq = nkv if rng.random() < 0.5 else int(rng.integers(1, nkv + 1))
+    shape = (H, nq, nkv) if rng.random() < 0.5 else (nq, nkv)
+    mask = (rng.random(shape) < 0.7).astype(np.uint8)
+    q = synth.tensor_bf16(4000 + seed, synth.TAG_Q, B, H, nq * bs, D)
+    k = synth.tensor_bf16(4000 + seed, synth.TAG_K, B, H, nkv * bs, D).copy()
+    v = synth.tensor_bf16(4000 + seed, synth.TAG_V, B, H, nkv * bs, D)
+    for _ in range(int(rng.integers(1, 4))):
+        b, h, j = int(rng.integers(0, B)), int(rng.integers(0, H)), int(rng.integers(0, nkv * bs))
+        f = 10.0 ** rng.uniform(0.5, 4.0)
+        k[b, h, j] = synth.f32_to_bf16_bits((synth.bf16_bits_to_f64(k[b, h, j]) * f).astype(np.float32))
+    scale = float(np.float32(1 / np.sqrt(D)))
+    what = f"loose {seed}: D{D} {B}x{H} {nq}/{nkv}x{bs} mask{shape}"
+    res = full_case(ba, q, k, v, mask, bs, scale, what=what)
+    must, may, _, online = _predicted_flags(q, k, v, mask, bs, scale, eligible=64.0)
+    L = nq * bs
+    r = np.arange(B * H * L)
+    upb = (bs + 255) // 256
+    unit_of_row = ((r // L) * nq + (r % L) // bs) * upb + (r % bs) // 256
+    n_units = B * H * nq * upb
+    want_online = len(np.unique(unit_of_row[online]))
+    assert res["online_units"] == want_online, what
+    assert res["bound_units"] == n_units - want_online, what
+    assert must <= res["fb_rows"] <= may, what
+
+
 @pytest.mark.parametrize("flags", [1, 2, 4, 6])
 def test_variants_small(ba, flags):
     w = synth.WORKLOADS["small"]
