@@ -178,7 +178,11 @@ bsattn_status setup_device(bsattn_layout_s &lay) {
     const size_t ntiles = std::max<size_t>(lay.tiles.size() / 2, 1);
     lay.grid = std::max(1, std::min(lay.n_units, lay.num_sms));
     std::vector<int32_t> slots;
-    lay.n_slots = bsv::schedule_units(lay, lay.grid, slots);
+    try {
+        lay.n_slots = bsv::schedule_units(lay, lay.grid, slots);
+    } catch (const std::bad_alloc &) {
+        return BSATTN_ERR_OOM;
+    }
     const size_t ws_ints = kWsHeader + 3 * static_cast<size_t>(lay.n_slots);
     if ((e = cudaMalloc(&lay.d_row_ptr, lay.row_ptr.size() * 4)) != cudaSuccess ||
         (e = cudaMalloc(&lay.d_col_idx, nnz * 4)) != cudaSuccess ||

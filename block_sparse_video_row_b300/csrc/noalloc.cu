@@ -20,6 +20,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "bsattn.h"
@@ -112,7 +113,13 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     bsattn_layout_info(plan, &info);
     const int grid = std::max(1, std::min(info.n_units, ds->num_sms));
     std::vector<int32_t> slots;
-    const int32_t n_slots = bsv::schedule_units(*plan, grid, slots);
+    int32_t n_slots = 0;
+    try {
+        n_slots = bsv::schedule_units(*plan, grid, slots);
+    } catch (const std::bad_alloc &) {
+        bsattn_destroy(plan);
+        return BSATTN_ERR_OOM;
+    }
     const size_t n = static_cast<size_t>(n_slots);
     const size_t ntiles = static_cast<size_t>(info.key_tiles > 0 ? info.key_tiles : 1);
 
@@ -129,7 +136,13 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
         bsattn_destroy(plan);
         return BSATTN_ERR_UNSUPPORTED;
     }
-    std::vector<unsigned char> host(total, 0);
+    std::vector<unsigned char> host;
+    try {
+        host.assign(total, 0);
+    } catch (const std::bad_alloc &) {
+        bsattn_destroy(plan);
+        return BSATTN_ERR_OOM;
+    }
     std::memcpy(host.data() + off_units, slots.data(), slots.size() * 4);
     bsattn_layout_export(plan, nullptr, nullptr, nullptr, reinterpret_cast<int32_t *>(host.data() + off_tileptr),
                          reinterpret_cast<int32_t *>(host.data() + off_tiles));

@@ -166,6 +166,9 @@ enum {
  * plus 150 per unit).  A device layout deals the units to its persistent CTAs
  * (one per SM) by that cost, each to the least-loaded CTA, in the order that
  * bsattn_layout_schedule describes.
+ * The plan follows the frame-aligned layout of the deep-dive's section 把 block 縮到 16
+ * (blocks whose edges are frame edges, any multiple of 16 tokens, so that no element
+ * predicate, tail pass or padding is needed).
  * Returns BSATTN_OK, INVALID_ARG, UNALIGNED_BLOCK, UNSUPPORTED, CUDA, OOM or DEVICE.
  */
 bsattn_status bsattn_create_layout(bsattn_layout_t *out, int32_t B, int32_t H, int64_t L, int32_t D,
@@ -340,7 +343,10 @@ bsattn_status bsattn_forward_noalloc(const void *q, const void *k, const void *v
 bsattn_status bsattn_noalloc_query(int64_t *fallback_rows, int64_t *fallback_units, int32_t *device_status,
                                    bsattn_stream_t stream);
 
-/* Free the layout's device buffers and host plan.  NULL is ignored. */
+/* Free the layout's device buffers (plan tables, workspace, the host-tensor path's staging
+ * and streams) and its host plan: the end of the layout created for one chunk shape and
+ * frame mask (deep-dive, section 把 block 縮到 16).  Synchronises the layout's own
+ * streams; work the caller queued on other streams must be complete.  NULL is ignored. */
 void bsattn_destroy(bsattn_layout_t lay);
 
 /* ---- helpers ----------------------------------------------------------------------------- */
