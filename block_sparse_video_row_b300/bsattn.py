@@ -54,7 +54,8 @@ class LayoutInfo(ctypes.Structure):
                 ("nnz_blocks", ctypes.c_int32), ("kv_tile", ctypes.c_int32), ("key_tiles", ctypes.c_int32),
                 ("q_tiles_per_block", ctypes.c_int32), ("n_units", ctypes.c_int32),
                 ("mma_rows", ctypes.c_int64), ("useful_flop", ctypes.c_double), ("L_kv", ctypes.c_int64),
-                ("nb_kv", ctypes.c_int32), ("mask_heads", ctypes.c_int32)]
+                ("nb_kv", ctypes.c_int32), ("mask_heads", ctypes.c_int32), ("n_segments", ctypes.c_int32),
+                ("tail_units", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -371,14 +372,15 @@ def bsattn_layout_schedule(lay: Layout, grid: int) -> np.ndarray:
 
 def bsattn_layout_export(lay: Layout, with_tiles: bool = False):
     """(row_ptr [mask_heads*nb+1], col_idx [nnz], units [n_units, 4]) as int32 numpy arrays; with_tiles
-    adds (tile_ptr [mask_heads*nb+1], tiles [key_tiles, 2]).  Segment m*nb + qb is query block qb of
-    mask m (m = 0 for a shared mask, the head for per-head masks)."""
+    adds (tile_ptr [n_segments+1], tiles [key_tiles, 2]).  Segment m*nb + qb is query block qb of
+    mask m (m = 0 for a shared mask, the head for per-head masks); segments from mask_heads*nb on are
+    packed-tail tiles, whose tiles' width words carry the allowed row groups in bits 16.."""
     i = lay.info
     nseg = max(1, i.mask_heads) * i.nb  # (mask, query block) segments
     row_ptr = np.zeros(nseg + 1, np.int32)
     col_idx = np.zeros(max(i.nnz_blocks, 1), np.int32)
     units = np.zeros((i.n_units, 4), np.int32)
-    tile_ptr = np.zeros(nseg + 1, np.int32)
+    tile_ptr = np.zeros(max(i.n_segments, nseg) + 1, np.int32)
     tiles = np.zeros((max(i.key_tiles, 1), 2), np.int32)
     _check(load().bsattn_layout_export(lay.handle, row_ptr.ctypes.data, col_idx.ctypes.data, units.ctypes.data,
                                        tile_ptr.ctypes.data, tiles.ctypes.data), "bsattn_layout_export")

@@ -64,40 +64,125 @@ void build_plan(bsattn_layout_s &lay, const uint8_t *mask) {
         lay.tile_ptr[sg + 1] = static_cast<int32_t>(lay.tiles.size() / 2);
     }
 
-    // Cost model (in hundredths of a two-tile key tile): a unit of two query tiles takes
-    // 100 per key tile; a unit of one tile 83, because its softmax cannot overlap another
-    // tile's MMAs; plus 150 per unit (query loads, epilogue).
-    struct Unit {
-        int32_t bh, qb, qt0, nt;
-        int64_t cost;
+    // Tail groups.  A frame of an odd number of query tiles whose last tile holds at most
+    // half a tile of rows (a 3600-token frame: 28 full tiles and 16 rows) leaves that tail
+    // as a unit of its own, which costs a whole tile's pass over the frame's key tiles for
+    // a few rows.  The tails of consecutive frames are packed into one query tile instead
+    // (row group g = frame qb0 + g, rows [g * tail_rows, (g + 1) * tail_rows)), as long as
+    // each added frame costs fewer key tiles than its own unit would: the packed tile reads
+    // every key frame any of its frames reads, cut into tiles at frame edges so that each
+    // key tile belongs to one frame, and each tile carries the set of row groups allowed to
+    // read it (bits 16.. of its width word); the kernel gives the other rows a shift of
+    // -inf for that tile, so their P is exactly 0.  No element mask is needed: a row reads
+    // whole key frames or nothing, as in every other unit.
+    const int32_t qt = lay.qt_per_block;
+    const int32_t tail_row0 = (qt - 1) * bsv::kQTile;
+    const int32_t tail_rows = lay.bs - tail_row0;
+    const bool grouping = qt % 2 == 1 && 2 * tail_rows <= bsv::kQTile;
+    const int32_t max_group = grouping ? std::min(bsv::kMaxTailGroup, bsv::kQTile / tail_rows) : 1;
+    const int64_t tiles_per_frame = (lay.bs + bsv::kKvTile - 1) / bsv::kKvTile;
+    struct Group {
+        int32_t qb0, n, seg;
     };
-    std::vector<Unit> us;
+    std::vector<std::vector<Group>> groups(static_cast<size_t>(lay.mask_heads));
+    std::vector<int32_t> in_group(static_cast<size_t>(nseg), 0);  // frame's tail is in a packed tile
+    int32_t n_seg_all = nseg;
+    for (int32_t m = 0; m < lay.mask_heads && grouping; ++m) {
+        int32_t qb = 0;
+        while (qb < nb) {
+            const int32_t s0 = m * nb + qb;
+            if (lay.row_ptr[s0 + 1] == lay.row_ptr[s0]) {  // reads nothing: its own unit writes zeros
+                ++qb;
+                continue;
+            }
+            std::vector<uint8_t> uni(static_cast<size_t>(nbkv), 0);
+            for (int32_t e = lay.row_ptr[s0]; e < lay.row_ptr[s0 + 1]; ++e) uni[lay.col_idx[e]] = 1;
+            int64_t n_uni = lay.row_ptr[s0 + 1] - lay.row_ptr[s0];      // key frames of the union
+            int64_t own_sum = lay.tile_ptr[s0 + 1] - lay.tile_ptr[s0];  // the members' own tail units
+            int32_t n = 1;
+            while (n < max_group && qb + n < nb) {
+                const int32_t s1 = m * nb + qb + n;
+                if (lay.row_ptr[s1 + 1] == lay.row_ptr[s1]) break;
+                int64_t added = 0;
+                for (int32_t e = lay.row_ptr[s1]; e < lay.row_ptr[s1 + 1]; ++e) added += uni[lay.col_idx[e]] ? 0 : 1;
+                const int64_t own = lay.tile_ptr[s1 + 1] - lay.tile_ptr[s1];
+                // the packed tile (frame-cut tiles of the union) must stay cheaper than the
+                // members' own tail units together
+                if ((n_uni + added) * tiles_per_frame >= own_sum + own) break;
+                for (int32_t e = lay.row_ptr[s1]; e < lay.row_ptr[s1 + 1]; ++e) uni[lay.col_idx[e]] = 1;
+                n_uni += added;
+                own_sum += own;
+                ++n;
+            }
+            if (n >= 2) {
+                const int32_t seg = n_seg_all++;
+                for (int32_t kb = 0; kb < nbkv; ++kb) {
+                    if (!uni[kb]) continue;
+                    int32_t rows = 0;  // row groups allowed to read key frame kb
+                    for (int32_t g = 0; g < n; ++g)
+                        if (mask[static_cast<int64_t>(m * nb + qb + g) * nbkv + kb]) rows |= 1 << g;
+                    const int64_t k0 = static_cast<int64_t>(kb) * lay.bs, k1 = k0 + lay.bs;
+                    for (int64_t k = k0; k < k1; k += bsv::kKvTile) {
+                        lay.tiles.push_back(static_cast<int32_t>(k));
+                        lay.tiles.push_back(static_cast<int32_t>(std::min<int64_t>(bsv::kKvTile, k1 - k)) |
+                                            (rows << 16));
+                    }
+                }
+                lay.tile_ptr.push_back(static_cast<int32_t>(lay.tiles.size() / 2));
+                groups[m].push_back({qb, n, seg});
+                for (int32_t g = 0; g < n; ++g) in_group[m * nb + qb + g] = 1;
+            }
+            qb += n;
+        }
+    }
+    lay.n_segments = n_seg_all;
+    lay.tail_units = 0;
+
+    // Cost model (in hundredths of a two-tile key tile): a unit of two query tiles takes
+    // 100 per key tile; a unit of one tile (a frame's lone tail, or packed tails) 83,
+    // because its softmax cannot overlap another tile's MMAs; plus 150 per unit (query
+    // loads, epilogue).  Units are listed in (head, frame, tile) order, a packed tile
+    // after the last frame of its group; schedule_units orders and deals them.
     const int32_t BH = lay.B * lay.H;
-    us.reserve(static_cast<size_t>(BH) * nb * ((lay.qt_per_block + 1) / 2));
-    int64_t mma_frames = 0, allowed_pairs = 0;  // over the B * H sequences
-    for (int32_t bh = 0; bh < BH; ++bh)
+    std::vector<int32_t> &U = lay.units;
+    U.clear();
+    lay.unit_cost.clear();
+    U.reserve(static_cast<size_t>(BH) * nb * ((qt + 1) / 2) * 4);
+    int64_t mma_tiles = 0, allowed_pairs = 0;  // over the B * H sequences
+    auto push = [&](int32_t x, int32_t y, int32_t z, int32_t w, int64_t cost, int64_t tiles_through_mma) {
+        U.push_back(x);
+        U.push_back(y);
+        U.push_back(z);
+        U.push_back(w);
+        lay.unit_cost.push_back(cost);
+        mma_tiles += tiles_through_mma;
+    };
+    for (int32_t bh = 0; bh < BH; ++bh) {
+        const int32_t m = lay.mask_heads > 1 ? bh % lay.H : 0;
+        size_t next_group = 0;
         for (int32_t qb = 0; qb < nb; ++qb) {
             const int sg = bsv::plan_segment(lay.mask_heads, lay.H, nb, bh, qb);
             const int64_t ntile = lay.tile_ptr[sg + 1] - lay.tile_ptr[sg];
             allowed_pairs += lay.row_ptr[sg + 1] - lay.row_ptr[sg];
-            mma_frames += lay.row_ptr[sg + 1] > lay.row_ptr[sg] ? 1 : 0;
-            for (int32_t qt0 = 0; qt0 < lay.qt_per_block; qt0 += 2) {
-                const int32_t nt = std::min(2, lay.qt_per_block - qt0);
-                us.push_back({bh, qb, qt0, nt, ntile * (nt == 2 ? 100 : 83) + 150});
+            const int64_t reads = ntile > 0 ? 1 : 0;
+            for (int32_t qt0 = 0; qt0 < qt; qt0 += 2) {
+                const int32_t nt = std::min(2, qt - qt0);
+                if (nt == 1 && in_group[m * nb + qb]) continue;  // its tail rides in a packed tile
+                push(bh, qb, qt0, nt, ntile * (nt == 2 ? 100 : 83) + 150, reads * nt);
+            }
+            if (next_group < groups[m].size()) {
+                const Group &gr = groups[m][next_group];
+                if (qb == gr.qb0 + gr.n - 1) {
+                    const int64_t gt = lay.tile_ptr[gr.seg + 1] - lay.tile_ptr[gr.seg];
+                    push(bh, gr.qb0, gr.seg, -gr.n, gt * 83 + 150, 1);
+                    ++lay.tail_units;
+                    ++next_group;
+                }
             }
         }
-    // Units stay in (head, frame, tile) order; schedule_units orders and deals them.
-    lay.n_units = static_cast<int32_t>(us.size());
-    lay.units.resize(us.size() * 4);
-    lay.unit_cost.resize(us.size());
-    for (size_t i = 0; i < us.size(); ++i) {
-        lay.units[4 * i + 0] = us[i].bh;
-        lay.units[4 * i + 1] = us[i].qb;
-        lay.units[4 * i + 2] = us[i].qt0;
-        lay.units[4 * i + 3] = us[i].nt;
-        lay.unit_cost[i] = us[i].cost;
     }
-    lay.mma_rows = mma_frames * lay.qt_per_block * bsv::kQTile;
+    lay.n_units = static_cast<int32_t>(lay.unit_cost.size());
+    lay.mma_rows = mma_tiles * bsv::kQTile;
     lay.useful_flop =
         4.0 * static_cast<double>(allowed_pairs) * static_cast<double>(lay.bs) * static_cast<double>(lay.bs) * lay.D;
 }
@@ -306,6 +391,18 @@ bool encode_o_store_map(CUtensorMap *m, const AttnParams &p, int D) {
                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_q_tail_map(CUtensorMap *m, const AttnParams &p, int D) {
+    if (!encode_fn()) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.block),
+                                static_cast<cuuint64_t>(p.bh) * static_cast<cuuint64_t>(p.nb)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(D) * 2 * p.block};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tail_rows(p.block)), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.q), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_layout_maps(const bsattn_layout_s *lay, const void *q, const void *k, const void *v, CUtensorMap *tq,
                         CUtensorMap *tk, CUtensorMap *tv) {
     return encode_fn() && encode_q_map(tq, *lay, q) && encode_kv_map(tk, *lay, k) && encode_kv_map(tv, *lay, v);
@@ -425,6 +522,8 @@ bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, 
     p.tile_ptr = lay->d_tile_ptr;
     p.tiles = lay->d_tiles;
     p.n_tiles = static_cast<int32_t>(lay->tiles.size() / 2);
+    p.n_seg = lay->n_segments;
+    p.q = q;
     p.bh = lay->B * lay->H;
     p.heads = lay->H;
     p.mask_heads = lay->mask_heads;
@@ -544,6 +643,8 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
     info->L_kv = lay->Lkv;
     info->nb_kv = lay->nbkv;
     info->mask_heads = lay->mask_heads;
+    info->n_segments = lay->n_segments;
+    info->tail_units = lay->tail_units;
     return BSATTN_OK;
 }
 

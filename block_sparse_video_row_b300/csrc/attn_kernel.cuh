@@ -152,20 +152,26 @@ __device__ __forceinline__ bool fetch_unit_checked(const AttnParams &p, int i, i
     }
     if (ok) {
         U = p.units[u];
-        ok = U.w >= 0 && U.w <= 2;
-        if (ok && U.w > 0) {
-            ok = U.x >= 0 && U.x < p.bh && U.y >= 0 && U.y < p.nb && U.z >= 0 &&
-                 (static_cast<int64_t>(U.z) + U.w - 1) * kQTile < p.block;
+        ok = U.w >= -kMaxTailGroup && U.w <= 2 && U.w != -1;
+        if (ok && U.w != 0) {
+            if (U.w > 0)
+                ok = U.x >= 0 && U.x < p.bh && U.y >= 0 && U.y < p.nb && U.z >= 0 &&
+                     (static_cast<int64_t>(U.z) + U.w - 1) * kQTile < p.block;
+            else  // packed tails: frames U.y .. U.y - U.w - 1, segment U.z past the (mask, frame) ones
+                ok = U.x >= 0 && U.x < p.bh && U.y >= 0 && U.y - U.w <= p.nb &&
+                     U.z >= p.mask_heads * p.nb && U.z < p.n_seg && -U.w * tail_rows(p.block) <= kQTile;
             if (ok) {
-                const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+                const int sg = U.w > 0 ? plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y) : U.z;
                 const int a = p.tile_ptr[sg], b = p.tile_ptr[sg + 1];
                 ok = a >= 0 && a <= b && b <= p.n_tiles;
                 for (int t = a; ok && t < b; ++t) {
                     int2 T = p.tiles[t];
                     // testing only: the CTA's first unit sees its first key tile past the last key
                     if (p.debug_plant && t == a && i == static_cast<int>(blockIdx.x)) T.x = static_cast<int>(p.Lkv);
-                    ok = T.x >= 0 && (T.x & 15) == 0 && T.y >= 16 && T.y <= kKvTile && (T.y & 15) == 0 &&
-                         static_cast<int64_t>(T.x) + T.y <= p.Lkv;
+                    const int tw = tile_width(T);
+                    ok = T.x >= 0 && (T.x & 15) == 0 && tw >= 16 && tw <= kKvTile && (tw & 15) == 0 &&
+                         static_cast<int64_t>(T.x) + tw <= p.Lkv &&
+                         (U.w > 0 ? tile_row_groups(T) == 0 : tile_row_groups(T) < (1 << -U.w));
                 }
             }
         }
@@ -361,7 +367,7 @@ template <int D, bool ONLINE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                      const AttnParams p) {
+                      const __grid_constant__ CUtensorMap tm_qt, const AttnParams p) {
     using C = AttnCfg<D>;
     // Positions of this launch: the bound launch walks the schedule unless the route kernel
     // sent every unit online; the fallback launch walks the schedule when it sent some
@@ -435,22 +441,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 int u;
                 int4 U;
                 if (!fetch_unit(p, i, base, u, U, true)) continue;  // not this launch's, or rejected by the checks
-                const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+                if (U.w == 0) continue;  // an empty schedule slot
+                const bool tail = U.w < 0;
+                const int sg = tail ? U.z : plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
                 const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
-                if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
+                if (nkv == 0) continue;  // reads nothing
                 // testing only: the first unit's query tiles are never loaded, so the
                 // issuers' bounded waits run out and the CTA aborts and returns
-                const int n_q = (p.debug_stall && i == static_cast<int>(blockIdx.x)) ? 0 : U.w;
+                const int n_q = (p.debug_stall && i == static_cast<int>(blockIdx.x)) ? 0 : (tail ? 1 : U.w);
                 for (int t = 0; t < n_q && ok; ++t) {
                     uint32_t &qu = t ? q_uses1 : q_uses0;
                     ok = mbar_wait(bar.q_empty + t, (qu & 1) ^ 1, bar.abort, status, kStatusTimeout, tmo);
                     if (!ok) break;
                     ++qu;
-                    mbar_arrive_expect_tx(bar.q_full + t, C::Q_TILE);
+                    if (tail) {
+                        // packed tails: row group g holds the tail rows of frame U.y + g; rows past
+                        // the last group keep stale data, which the softmax gives P = 0
+                        const int tr = tail_rows(p.block);
+                        mbar_arrive_expect_tx(bar.q_full, -U.w * tr * 128 * C::DH);
+                        for (int gq = 0; gq < -U.w; ++gq)
 #pragma unroll
-                    for (int h = 0; h < C::DH; ++h)
-                        tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + h * C::HALF_Q, &tm_q, h * 64,
-                                    (U.z + t) * kQTile, U.x * p.nb + U.y, bar.q_full + t, pol_q);
+                            for (int h = 0; h < C::DH; ++h)
+                                tma_load_3d(smem + C::OFF_Q + h * C::HALF_Q + gq * tr * 128, &tm_qt, h * 64,
+                                            tail_row0(p.block), U.x * p.nb + U.y + gq, bar.q_full, pol_q);
+                    } else {
+                        mbar_arrive_expect_tx(bar.q_full + t, C::Q_TILE);
+#pragma unroll
+                        for (int h = 0; h < C::DH; ++h)
+                            tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + h * C::HALF_Q, &tm_q, h * 64,
+                                        (U.z + t) * kQTile, U.x * p.nb + U.y, bar.q_full + t, pol_q);
+                    }
                 }
                 for (int j = 0; j < nkv && ok; ++j, ++g) {
                     const int row = static_cast<int>(static_cast<int64_t>(U.x) * p.Lkv) + p.tiles[t0 + j].x;
@@ -523,10 +543,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 int u;
                 int4 U;
                 if (!fetch_unit(p, i, base, u, U, false)) continue;  // not this launch's, or rejected by the checks
-                const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+                if (U.w == 0) continue;  // an empty schedule slot
+                const int sg = U.w < 0 ? U.z : plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
                 const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
-                if (nkv == 0 || U.w == 0) continue;  // reads nothing, or an empty schedule slot
-                if (t >= U.w) {
+                if (nkv == 0) continue;  // reads nothing
+                if (t >= (U.w < 0 ? 1 : U.w)) {
                     // This query tile is absent from the unit: release each stage without MMAs,
                     // after its copy has landed (so the arrival counts toward the right phase).
                     for (int j = 0; j < nkv && ok; ++j) {
@@ -546,7 +567,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ok = mbar_wait(bar.q_full + t, q_uses & 1, bar.abort, status, kStatusTimeout, tmo);
                 ++q_uses;
                 if (!ok) break;
-                int w_next = p.tiles[t0].y;
+                int w_next = tile_width(p.tiles[t0]);
                 {
                     const int s0 = static_cast<int>(g % C::STAGES);
                     ok = mbar_wait(bar.k_full + s0, (g / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
@@ -562,7 +583,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int sj = static_cast<int>(gj % C::STAGES), sn = static_cast<int>(gn % C::STAGES);
                     const bool more = j + 1 < nkv;
                     const int wj = w_next;
-                    if (more) w_next = p.tiles[t0 + j + 1].y;
+                    if (more) w_next = tile_width(p.tiles[t0 + j + 1]);
                     ok = mbar_wait(bar.v_full + sj, (gj / C::STAGES) & 1, bar.abort, status, kStatusTimeout, tmo);
                     if (ok && more)
                         ok = mbar_wait(bar.k_full + sn, (gn / C::STAGES) & 1, bar.abort, status, kStatusTimeout,
@@ -620,14 +641,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             int u;
             int4 U;
             if (!fetch_unit(p, i, base, u, U, false)) continue;  // not this launch's, or rejected by the checks
-            const int nt = U.w;
-            if (nt == 0) continue;  // an empty schedule slot
-            const int sg = plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
+            if (U.w == 0) continue;  // an empty schedule slot
+            const bool tail = U.w < 0;
+            const int nt = tail ? 1 : U.w;
+            const int sg = tail ? U.z : plan_segment(p.mask_heads, p.heads, p.nb, U.x, U.y);
             const int t0 = p.tile_ptr[sg], nkv = p.tile_ptr[sg + 1] - t0;
-            const int64_t row0 = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
-                                 static_cast<int64_t>(U.z) * kQTile + r;  // this thread's row of tile 0
-            const bool valid0 = r < min(kQTile, p.block - U.z * kQTile);
-            const bool valid1 = nt > 1 && r < min(kQTile, p.block - (U.z + 1) * kQTile);
+            // This thread's row of tile 0.  Packed tails: row r is in row group r / tail_rows,
+            // the tail of frame U.y + group; rowbit marks its group in the key tiles' masks
+            // (rows past the last group match no mask and keep P = 0 on every tile).
+            int64_t row0;
+            bool valid0, valid1;
+            uint32_t rowbit = 0;
+            if (tail) {
+                const int tr = tail_rows(p.block), grp = r / tr;
+                valid0 = grp < -U.w;
+                valid1 = false;
+                rowbit = valid0 ? 1u << grp : 0u;
+                row0 = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y + grp) * p.block + tail_row0(p.block) +
+                       (r - grp * tr);
+            } else {
+                row0 = static_cast<int64_t>(U.x) * p.L + static_cast<int64_t>(U.y) * p.block +
+                       static_cast<int64_t>(U.z) * kQTile + r;
+                valid0 = r < min(kQTile, p.block - U.z * kQTile);
+                valid1 = nt > 1 && r < min(kQTile, p.block - (U.z + 1) * kQTile);
+            }
             if (nkv == 0) {  // the frame reads no key block: O = 0, LSE = -inf
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
@@ -655,9 +692,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             uint64_t nm1 = f2_make(-mrow1 * 1.4426950408889634f, -mrow1 * 1.4426950408889634f);
             // row-sum accumulators: key 4i + k of a half goes to lt[k]
             float lt0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, lt1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint64_t ninf2 = f2_make(-INFINITY, -INFINITY);
             for (int j = 0; j < nkv && ok; ++j) {
-                const int w = p.tiles[t0 + j].y;
+                const int2 T = p.tiles[t0 + j];
+                const int w = tile_width(T);
                 const int wh = max(0, min(64, w - 64 * h));
+                // packed tails: a row whose frame may not read this key tile gets a shift of -inf
+                // for it (P = 0, and no effect on its running max)
+                const bool allowed = !tail || (static_cast<uint32_t>(tile_row_groups(T)) & rowbit) != 0;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (t >= nt) break;
@@ -676,7 +718,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if constexpr (ONLINE) {
                         float &mrow = t ? mrow1 : mrow0;
                         float other;
-                        const float mine = load_half_max(tS, wh, sbuf) * c1;
+                        float mine = load_half_max(tS, wh, sbuf) * c1;  // warp-collective load
+                        if (!allowed) mine = -INFINITY;
                         ok = pair_exchange(bar, q, h, r, x_uses, mine, other, status, tmo);
                         if (!ok) break;
                         const float mx = fmaxf(mine, other);
@@ -704,7 +747,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar.p_full + t);
                     };
-                    softmax_half<ONLINE>(tS, wh, c1x2, nm, lt, sbuf, handoff);
+                    softmax_half<ONLINE>(tS, wh, c1x2, allowed ? nm : ninf2, lt, sbuf, handoff);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -748,6 +791,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         float x0, x1;
                         f2_split(f2_mul(f2_from_bits(a[2 * e], a[2 * e + 1]), inv2), x0, x1);
                         wv[e] = pack_bf16x2(x0, x1);
+                    }
+                    if (tail) {  // packed tails: this warp's rows lie in several frames
+                        if (valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D + DC * h + 32 * c);
+                            dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                            dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                            dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+                            dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+                        }
+                        continue;
                     }
                     if (ost_busy) {  // the previous store must have read the staging buffer
                         if (lane == 0) bulk_wait_read0();
@@ -805,9 +858,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D, bool ONLINE>
 cudaError_t launch_fwd_instance(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const AttnParams &p, int n_ctas, cudaStream_t s) {
-    CUtensorMap to;
-    if (!encode_o_store_map(&to, p, D)) return cudaErrorInvalidValue;
-    bsattn_fwd_kernel<D, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D>::SMEM, s>>>(tq, tk, tv, to, p);
+    CUtensorMap to, tqt;
+    if (!encode_o_store_map(&to, p, D) || !encode_q_tail_map(&tqt, p, D)) return cudaErrorInvalidValue;
+    bsattn_fwd_kernel<D, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D>::SMEM, s>>>(tq, tk, tv, to, tqt, p);
     return cudaGetLastError();
 }
 

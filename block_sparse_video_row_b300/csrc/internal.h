@@ -11,6 +11,7 @@ namespace bsv {
 
 constexpr int kQTile = 128;           // query rows per tile (the MMA M dimension)
 constexpr int kKvTile = 128;          // keys per full key tile (TMEM: 2 S + 2 O accumulators of 128 columns)
+constexpr int kMaxTailGroup = 8;      // frames whose tails share one packed query tile (mask bits 16..23)
 constexpr int kAttnThreads = 384;     // 12 warps: TMA, MMA, 2 idle, 2 softmax warpgroups
 constexpr int kLaunchRegs = 168;      // registers per thread at launch (65536 / 384, rounded down to 8)
 constexpr int kRegsLow = 72;          // TMA / MMA warpgroup after setmaxnreg.dec
@@ -57,11 +58,15 @@ enum AttnMode : int32_t {
 };
 
 struct AttnParams {
-    const int4 *units;        // (b*H + h, qb, first q tile, tiles in unit)
+    const int4 *units;        // (b*H + h, qb, first q tile, tiles in unit: 1 or 2), or for packed
+                              // tails (b*H + h, first frame, segment, -frames)
     int32_t n_units;
-    const int32_t *tile_ptr;  // key tiles of query block qb: tiles[tile_ptr[qb] .. tile_ptr[qb+1])
-    const int2 *tiles;        // (first key within the head, width: a multiple of 16, <= kKvTile)
+    const int32_t *tile_ptr;  // key tiles of segment s: tiles[tile_ptr[s] .. tile_ptr[s+1])
+    const int2 *tiles;        // (first key within the head, width: a multiple of 16, <= kKvTile,
+                              //  | row groups allowed << 16 for the tiles of a packed-tail segment)
     int32_t n_tiles;          // entries of tiles
+    int32_t n_seg;            // segments (entries of tile_ptr minus one)
+    const void *q;            // Q (bf16): the packed-tail loads use their own tensor map
     int32_t bh;               // B * H
     int32_t heads;            // H
     int32_t mask_heads;       // block masks: 1 (shared by all heads) or H (mask h for head h)
@@ -95,6 +100,14 @@ struct BoundsParams {
     float scale;
 };
 
+// Width and allowed row groups of a key tile.
+__host__ __device__ __forceinline__ int tile_width(int2 t) { return t.y & 0xFFFF; }
+__host__ __device__ __forceinline__ int tile_row_groups(int2 t) { return static_cast<int>(static_cast<uint32_t>(t.y) >> 16); }
+
+// Rows of a frame's last query tile, and its first row, for frames of `block` tokens.
+__host__ __device__ __forceinline__ int tail_row0(int block) { return (block - 1) / kQTile * kQTile; }
+__host__ __device__ __forceinline__ int tail_rows(int block) { return block - tail_row0(block); }
+
 // Segment of the plan's tables (row_ptr, tile_ptr) for query block qb of sequence bh
 // (= b * H + h): mask m = h of a per-head plan (0 for a shared mask), segment m * nb + qb.
 __host__ __device__ __forceinline__ int plan_segment(int mask_heads, int heads, int nb, int64_t bh, int qb) {
@@ -105,6 +118,9 @@ __host__ __device__ __forceinline__ int plan_segment(int mask_heads, int heads, 
 // B*H*nb frames), box 32 columns x 32 rows, 64-byte swizzle.  False if the driver entry
 // point is missing or the driver rejects the map.
 bool encode_o_store_map(CUtensorMap *m, const AttnParams &p, int D);
+// TMA map for the Q loads of packed tails (built per launch from p.q): the frame layout of Q
+// with a box of tail_rows(block) rows, so each frame's tail lands in its own row group.
+bool encode_q_tail_map(CUtensorMap *m, const AttnParams &p, int D);
 
 // Launchers (return the launch error, if any).
 // The eligibility check of every schedule slot before the forward's two launches: a

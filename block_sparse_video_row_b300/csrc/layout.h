@@ -30,6 +30,8 @@ struct bsattn_layout_s {
     std::vector<int32_t> row_ptr, col_idx, units;
     std::vector<int32_t> tile_ptr, tiles;  // tiles: (first key within the head, width) pairs
     int32_t kv_tile = 0, qt_per_block = 0, n_units = 0;
+    int32_t n_segments = 0;  // segments of tile_ptr: masks * nb, then one per packed tail tile
+    int32_t tail_units = 0;  // units that are packed tails of several frames
     std::vector<int64_t> unit_cost;  // cost model of each unit of `units`
     int32_t grid = 0, n_slots = 0;   // persistent CTAs and scheduled slots (device layouts)
     int64_t mma_rows = 0;

@@ -129,8 +129,7 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     // array are rejected here, before any device work.
     const size_t off_units = align256((bsv::kWsHeaderInts + 3 * n) * 4);
     const size_t off_tileptr = align256(off_units + 16 * n);
-    const size_t off_tiles =
-        align256(off_tileptr + 4 * (static_cast<size_t>(info.mask_heads) * static_cast<size_t>(info.nb) + 1));
+    const size_t off_tiles = align256(off_tileptr + 4 * (static_cast<size_t>(info.n_segments) + 1));
     const size_t total = off_tiles + 8 * ntiles;
     if (total > kNoallocScratchBytes) {
         bsattn_destroy(plan);
@@ -170,6 +169,8 @@ extern "C" bsattn_status bsattn_forward_noalloc(const void *q, const void *k, co
     p.tile_ptr = reinterpret_cast<const int32_t *>(base + off_tileptr);
     p.tiles = reinterpret_cast<const int2 *>(base + off_tiles);
     p.n_tiles = info.key_tiles;
+    p.n_seg = info.n_segments;
+    p.q = q;
     p.bh = info.B * info.H;
     p.heads = info.H;
     p.mask_heads = info.mask_heads;

@@ -161,7 +161,13 @@ enum {
  * an exactly sized MMA with no element mask or padding and none reaches into a
  * masked frame); query tiles of 128 rows that never straddle a frame edge (the
  * last tile of a frame may be partial); and a work list of pairs of query
- * tiles of one frame with a cost each (100 per key tile for a unit of two query
+ * tiles of one frame.  When a frame has an odd number of query tiles and its
+ * last one holds at most 64 rows (a 3600-token frame: 28 tiles and 16 rows),
+ * the tails of up to 8 consecutive frames are packed into one query tile (row
+ * group g = the g-th frame) while each added frame costs fewer key tiles than
+ * its own tail unit: that tile reads every key frame of its frames, in tiles cut
+ * at frame edges, each marked with the row groups allowed to read it (a row
+ * still reads exactly its own frames).  Every unit has a cost (100 per key tile for a unit of two query
  * tiles, 83 for one tile, whose softmax cannot overlap another tile's MMAs,
  * plus 150 per unit).  A device layout deals the units to its persistent CTAs
  * (one per SM) by that cost, each to the least-loaded CTA, in the order that
@@ -311,8 +317,9 @@ bsattn_status bsattn_forward_host(bsattn_layout_t lay, const void *q, const void
  * Limits: the array holds an 8-int guard header, 28 bytes per schedule slot (16 for
  * the slot, 4 each for its guard flag, its fallback-list entry and its eligibility;
  * the slots are the work units dealt to the CTAs, padded with empty slots to a
- * multiple of the SM count), the key-tile index of 4 * (masks * nb + 1) bytes and
- * 8 bytes per key tile, each of the four parts rounded up to 256 bytes.  That is
+ * multiple of the SM count), the key-tile index of 4 * (n_segments + 1) bytes
+ * (bsattn_layout_info) and 8 bytes per key tile, each of the four parts rounded up to
+ * 256 bytes.  That is
  * about 37,000 slots (the 720p chunk uses about 4,700, the 1080p chunk about
  * 10,000); a larger problem returns BSATTN_ERR_UNSUPPORTED before any device work.
  * The first call on a device (with that device current) looks up the array's
@@ -393,6 +400,8 @@ typedef struct {
     int64_t L_kv;              /* key tokens per sequence (L for self-attention) */
     int32_t nb_kv;             /* key blocks */
     int32_t mask_heads;        /* masks in the plan: 1, or H with BSATTN_MASK_PER_HEAD */
+    int32_t n_segments;        /* key-tile segments: mask_heads * nb, then one per packed-tail tile */
+    int32_t tail_units;        /* work units that are packed tails of several frames (see create) */
 } bsattn_layout_info_t;
 
 bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info);
@@ -403,9 +412,13 @@ bsattn_status bsattn_layout_info(bsattn_layout_t lay, bsattn_layout_info_t *info
  *   row_ptr  int32 [mask_heads * nb + 1], col_idx int32 [nnz_blocks]: allowed key blocks of
  *            segment s in col_idx[row_ptr[s] .. row_ptr[s+1]), ascending;
  *   units    int32 [n_units * 4]: (b * H + h, query block, first query tile, tiles in the unit (1 or 2)),
- *            in (b * H + h, query block, first query tile) order;
- *   tile_ptr int32 [mask_heads * nb + 1], tiles int32 [key_tiles * 2]: the key tiles of segment s are
- *            (tiles[2t], tiles[2t+1]) = (first key within the head, width) for t in [tile_ptr[s], tile_ptr[s+1]).
+ *            in (b * H + h, query block, first query tile) order; a packed-tail unit (see
+ *            bsattn_create_layout) is (b * H + h, first frame, its segment, -frames) and follows the
+ *            units of its last frame;
+ *   tile_ptr int32 [n_segments + 1], tiles int32 [key_tiles * 2]: the key tiles of segment s are
+ *            (tiles[2t], tiles[2t+1]) = (first key within the head, width) for t in [tile_ptr[s], tile_ptr[s+1]);
+ *            segments from mask_heads * nb on are packed-tail tiles, whose width words carry in bits
+ *            16..23 the row groups (frames) allowed to read the tile.
  */
 bsattn_status bsattn_layout_export(bsattn_layout_t lay, int32_t *row_ptr, int32_t *col_idx, int32_t *units,
                                    int32_t *tile_ptr, int32_t *tiles);

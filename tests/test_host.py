@@ -51,6 +51,46 @@ def check_tiles(mask, bs, tile_ptr, tiles):
                 assert w == 128
 
 
+def check_units(masks, bs, H, units, tile_ptr, tiles, BH):
+    """Every (sequence, frame, query tile) exactly once.  A unit is 1 or 2 query tiles of one
+    frame, or a packed tile of frame tails (b*H+h, first frame, segment, -n): the last query
+    tile of frames qb0 .. qb0+n-1, reading the key tiles of its segment.  Those are cut at frame
+    edges, cover exactly the key frames any of its frames reads, and carry in bits 16.. of the
+    width the frames (row groups) allowed to read them.  Packing happens only for frames with an
+    odd number of query tiles and a tail of at most 64 rows, and only when cheaper than the
+    frames' own tail units."""
+    nb, nbkv = masks.shape[1], masks.shape[2]
+    nqt = -(-bs // 128)
+    tail_rows = bs - (nqt - 1) * 128
+    seen = np.zeros((BH, nb, nqt), np.int32)
+    for bh, qb, z, w in units:
+        if w > 0:
+            assert w in (1, 2) and z % 2 == 0 and z + w <= nqt
+            seen[bh, qb, z:z + w] += 1
+            continue
+        n = -w
+        assert nqt % 2 == 1 and 2 * tail_rows <= 128 and 2 <= n <= min(8, 128 // tail_rows)
+        m = masks[bh % H] if len(masks) > 1 else masks[0]
+        seen[bh, qb:qb + n, nqt - 1] += 1
+        assert z >= len(masks) * nb
+        t = tiles[tile_ptr[z]:tile_ptr[z + 1]]
+        width, groups = t[:, 1] & 0xFFFF, t[:, 1] >> 16
+        frames = t[:, 0] // bs
+        assert np.all(frames == (t[:, 0] + width - 1) // bs)        # within one frame
+        union = sorted({kb for g in range(n) for kb in range(nbkv) if m[qb + g, kb]})
+        assert list(np.unique(frames)) == union
+        for kb in union:                                            # each frame whole, in order
+            sel = t[frames == kb]
+            keys = np.concatenate([np.arange(a, a + (b & 0xFFFF)) for a, b in sel])
+            assert np.array_equal(keys, np.arange(kb * bs, (kb + 1) * bs))
+        for (a, _), gbits, kb in zip(t, groups, frames):
+            assert gbits == sum(1 << g for g in range(n) if m[qb + g, kb])
+        own = sum(tile_ptr[qb + g + 1] - tile_ptr[qb + g] for g in range(n)) if len(masks) == 1 else None
+        if own is not None:
+            assert len(t) < own                                     # cheaper than n own tail units
+    assert np.all(seen == 1)
+
+
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
 def test_plan_matches_oracle(lib, name):
     w = synth.WORKLOADS[name]
@@ -75,21 +115,19 @@ def test_plan_matches_oracle(lib, name):
     nqt = -(-w.block // 128)
     assert info.q_tiles_per_block == nqt
     assert abs(info.useful_flop - synth.useful_flop(w)) == 0
-    # every (head, frame, query tile) exactly once; units are 1 or 2 tiles of one frame
-    seen = np.zeros((w.B * w.H, w.nb, nqt), np.int32)
-    for bh, qb, qt0, nt in units:
-        assert nt in (1, 2) and qt0 % 2 == 0 and qt0 + nt <= nqt
-        seen[bh, qb, qt0:qt0 + nt] += 1
-    assert np.all(seen == 1)
-    # plan order: (head, frame, first query tile)
-    key = (units[:, 0].astype(np.int64) * w.nb + units[:, 1]) * nqt + units[:, 2]
+    check_units(masks, w.block, w.H, units, tile_ptr, tiles, w.B * w.H)
+    # plan order: (head, frame, first query tile), a packed tail after its last frame's units
+    last = np.where(units[:, 3] < 0, units[:, 1] - units[:, 3] - 1, units[:, 1])
+    pos = np.where(units[:, 3] < 0, nqt, units[:, 2])
+    key = (units[:, 0].astype(np.int64) * w.nb + last) * (nqt + 1) + pos
     assert np.all(np.diff(key) > 0)
     lay.destroy()
 
 
 def _unit_cost(units, tile_ptr, H, nb, per_head):
     # the documented model: 100 per key tile for a unit of two query tiles, 83 for one, plus 150
-    segment = (units[:, 0] % H if per_head else 0) * nb + units[:, 1]
+    # a packed tail (w < 0) reads the tiles of its own segment z, as one query tile
+    segment = np.where(units[:, 3] < 0, units[:, 2], (units[:, 0] % H if per_head else 0) * nb + units[:, 1])
     ntile = np.diff(tile_ptr)[segment]
     return ntile * np.where(units[:, 3] == 2, 100, 83) + 150
 
@@ -105,7 +143,7 @@ def test_schedule_deals_every_unit_once_head_major_then_by_cost(lib, name, grid)
     g = min(grid, n)
     slots = bsattn.bsattn_layout_schedule(lay, g)
     assert len(slots) % g == 0
-    real = slots[:, 3] > 0
+    real = slots[:, 3] != 0
     assert np.all(slots[~real] == 0)
     # every unit exactly once
     got = sorted(map(tuple, slots[real]))
@@ -323,11 +361,7 @@ def test_plan_matches_oracle_on_random_masks(lib):
         assert np.array_equal(row_ptr, orp) and np.array_equal(col_idx, oci), trial
         for mi, m in enumerate(masks):
             check_tiles(m, bs, tile_ptr[mi * nb:(mi + 1) * nb + 1], tiles)
-        nqt = -(-bs // 128)
-        seen = np.zeros((2 * H, nb, nqt), np.int32)
-        for bh, qb, qt0, nt in units:
-            seen[bh, qb, qt0:qt0 + nt] += 1
-        assert np.all(seen == 1), trial
+        check_units(masks, bs, H, units, tile_ptr, tiles, 2 * H)
         lay.destroy()
 
 
