@@ -394,7 +394,8 @@ def main():
                 "alone_ms_x_mhz": bound_avg * bound_mhz if bound_mhz else None},
             "guard": {"fallback_rows": fb_rows, "fallback_units": fb_units, "device_status": dev_status},
             "eligibility": {"bound_units": bound_units, "online_units": online_units},
-            "wasted_mma_rows_pct": 100.0 * (lay.info.mma_rows - B * H * L) / lay.info.mma_rows}
+            "wasted_mma_rows_pct": 100.0 * (lay.info.mma_rows - B * H * L) / lay.info.mma_rows,
+            "wasted_mma_work_pct": 100.0 * (1.0 - flop_step / (4.0 * D * mma_work(bsattn, lay)))}
 
     if rank == 0 and not args.no_cpu_baseline:
         tf, nrows, dt, cores = cpu_oracle_sample(q, k, v, w, args.cpu_seconds)
@@ -405,6 +406,22 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def mma_work(bsattn, lay) -> int:
+    """(query row, key) pairs the MMAs process per forward, from the plan: every unit runs 128
+    rows per query tile (zero rows of a partial tile included) against every key of its key
+    tiles; a packed tile of frame tails reads the union of its frames' key frames."""
+    import numpy as np
+    i = lay.info
+    _, _, units, tile_ptr, tiles = bsattn.bsattn_layout_export(lay, with_tiles=True)
+    keys_per_seg = np.add.reduceat(tiles[:, 1] & 0xFFFF, tile_ptr[:-1]) if len(tiles) else np.zeros(0)
+    keys_per_seg = np.where(np.diff(tile_ptr) > 0, keys_per_seg, 0)
+    H, nb = i.H, i.nb
+    per_head = i.mask_heads > 1
+    seg = np.where(units[:, 3] < 0, units[:, 2], (units[:, 0] % H if per_head else 0) * nb + units[:, 1])
+    tiles_q = np.where(units[:, 3] < 0, 1, units[:, 3])
+    return int(np.sum(128 * tiles_q * keys_per_seg[seg]))
 
 
 def bsattn_kernel_rev() -> str:

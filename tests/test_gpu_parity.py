@@ -499,6 +499,26 @@ def test_host_path_equals_device_path(ba, name, pairs, flags):
     lay.destroy()
 
 
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_host_path_with_packed_tails(ba, pairs):
+    # Frames with 16-row tails and one mask per head through the host-tensor path: each
+    # chunk's layout packs its heads' tails as the whole layout does, so the output is the
+    # device path's bit for bit, and the eligibility counts of the chunks add up to its counts.
+    q, k, v, mask, bs, scale = _tails_case(128, True, loose=True)
+    B, H, L, D = q.shape
+    lay = ba.bsattn_create_layout(B, H, L, D, bs, mask)
+    assert lay.info.tail_units > 0
+    dev = run_gpu(ba, q, k, v, mask, bs, scale, 0, want_meta=False, lay=lay)
+    hq, hk, hv = _pinned(q), _pinned(k), _pinned(v)
+    ho = torch.full_like(hq, float("nan")).pin_memory()
+    ba.bsattn_forward_host(lay, hq, hk, hv, ho, scale, None, 0, pairs)
+    torch.cuda.synchronize()
+    assert torch.equal(ho.view(torch.int16), dev["o_raw"].cpu().view(torch.int16))
+    assert ba.bsattn_query_eligibility(lay) == (dev["bound_units"], dev["online_units"])
+    assert dev["online_units"] > 0
+    lay.destroy()
+
+
 def test_bounded_wait_runs_out_and_the_context_stays_usable(ba, monkeypatch):
     # BSATTN_DEBUG_STALL withholds the first unit's query tiles in every CTA: the MMA
     # issuers' waits run out after the layout's 200 ms limit, the CTA aborts (copies in
