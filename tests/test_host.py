@@ -235,8 +235,41 @@ def test_plan_only_layout_refuses_device_calls(lib):
         bsattn.BSATTN_ERR_INVALID_ARG
     assert bsattn.bsattn_forward(lay, fake, fake, fake, fake, 0.125, fake, None, 0, 0, raise_on_error=False) == \
         bsattn.BSATTN_ERR_INVALID_ARG
+    assert bsattn.bsattn_row_bounds_from_norms(lay, fake, fake, 0.125, fake, fake, 0, raise_on_error=False) == \
+        bsattn.BSATTN_ERR_INVALID_ARG
     lay.destroy()
     lib.bsattn_destroy(None)  # NULL is ignored
+
+
+def test_new_entry_points_reject_bad_arguments(lib):
+    import ctypes
+    lay = bsattn.bsattn_create_layout(1, 2, 192, 64, 48, synth.window_mask(4, 1), bsattn.BSATTN_PLAN_ONLY)
+    n = ctypes.c_int32()
+    # the schedule needs a grid of at least one CTA and somewhere to put the slot count
+    assert lib.bsattn_layout_schedule(lay.handle, 0, None, ctypes.byref(n)) == bsattn.BSATTN_ERR_INVALID_ARG
+    assert lib.bsattn_layout_schedule(lay.handle, 4, None, None) == bsattn.BSATTN_ERR_INVALID_ARG
+    assert lib.bsattn_layout_schedule(None, 4, None, ctypes.byref(n)) == bsattn.BSATTN_ERR_INVALID_ARG
+    assert lib.bsattn_layout_schedule(lay.handle, 3, None, ctypes.byref(n)) == bsattn.BSATTN_OK
+    assert n.value % 3 == 0 and n.value >= lay.info.n_units
+    # eligibility counts need a device layout
+    b, o = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.bsattn_query_eligibility(lay.handle, ctypes.byref(b), ctypes.byref(o), None) == \
+        bsattn.BSATTN_ERR_INVALID_ARG
+    lay.destroy()
+
+
+def test_noalloc_entry_points_without_a_gpu_report_an_error(lib):
+    import ctypes
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rows, units, dev = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    st = lib.bsattn_noalloc_query(ctypes.byref(rows), ctypes.byref(units), ctypes.byref(dev), None)
+    assert st in (bsattn.BSATTN_ERR_DEVICE, bsattn.BSATTN_ERR_CUDA)
+    fake = 1 << 20  # never dereferenced: the device look-up fails first
+    st = bsattn.bsattn_forward_noalloc(fake, fake, fake, fake, 1, 2, 192, 64, 48, synth.window_mask(4, 1), 0.125,
+                                       fake, None, 0, raise_on_error=False)
+    assert st in (bsattn.BSATTN_ERR_DEVICE, bsattn.BSATTN_ERR_CUDA)
 
 
 def test_status_strings(lib):
