@@ -69,7 +69,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "25"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
