@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "useful TFLOP/s block-sparse attn fwd (bf16) on 1 B300; % of tensor peak"
 UNIT = "TFLOP/s"
+ALSO_DEFAULT = "720p_heads,stream,stress,1080p,1080p_dense"
 
 
 def _env_rank():
@@ -175,6 +176,9 @@ def main():
     ap.add_argument("--heads", type=int, default=0, help="override H (a smaller case of the same shape, for ncu)")
     ap.add_argument("--profile", action="store_true",
                     help="run only W warm-up and K timed steps (a short, fixed launch sequence for ncu)")
+    ap.add_argument("--also", default=ALSO_DEFAULT,
+                    help="comma-separated workloads measured after the headline one, in the same process "
+                         "(reported under also_measured; 'none' to skip; only with the 720p headline on 1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -402,10 +406,113 @@ def main():
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{nrows} random query rows of the {w.name} chunk, {dt:.1f} s fp64"}
     lay.destroy()
+    also = [x for x in args.also.split(",") if x and x != "none"]
+    if also and world == 1 and w.name == "720p":
+        del o, qn, km, rb, ho, hq, hk, hv
+        line["also_measured"] = measure_also(also, w, (dq, dk, dv), args.steps, local_rank, peak)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_also(names, main_w, main_dev, steps: int, gpu: int, peak: float) -> dict:
+    """The same step (bounds + default forward) on further workloads, each after a warm-up of at
+    least 0.5 s, with its own clock samples, plus one block of back-to-back default forwards and
+    one of online-max forwards.  Inputs equal to the headline workload's (same seed, shape and key
+    distribution) are taken from its device tensors; the rest are generated here."""
+    import torch
+    from block_sparse_video_row_b300 import bsattn, synth
+
+    def ident(x):
+        return (x.seed, x.B, x.H, x.L_kv, x.D, x.keys)
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+
+    cache = {ident(main_w): main_dev}
+    out = {"how": f"after the headline measurement, in the same process: {steps} timed steps of bounds + "
+                  "forward after a warm-up of >= 0.5 s, clocks binned per region; then one ~0.25 s block of "
+                  "default forwards and one of online-max forwards"}
+    stream = torch.cuda.current_stream()
+    for name in names:
+        w = synth.WORKLOADS[name]
+        key = ident(w)
+        if key not in cache:
+            cache = {k2: v2 for k2, v2 in cache.items() if k2 == ident(main_w)}  # keep the headline's only
+            torch.cuda.empty_cache()
+            cache[key] = tuple(dev(a) for a in synth.make_qkv(w))
+        fq, dk, dv = cache[key]
+        dq = fq if w.L == w.L_kv else fq[:, :, w.L_kv - w.L:].contiguous()
+        B, H, L, D = dq.shape
+        o = torch.empty_like(dq)
+        qn = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+        km = torch.empty((B, H, w.L_kv // w.block), dtype=torch.float32, device="cuda")
+        rb = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+        lay = bsattn.bsattn_create_layout(B, H, L, D, w.block, w.block_mask(), L_kv=w.L_kv)
+        flop = synth.useful_flop(w)
+
+        def fwd(fl):
+            bsattn.bsattn_forward(lay, dq, dk, dv, o, w.scale, rb, None, fl, stream)
+
+        def step(mid=None):
+            bsattn.bsattn_row_bounds(lay, dq, dk, w.scale, qn, km, rb, stream)
+            if mid is not None:
+                mid.record(stream)
+            fwd(bsattn.BSATTN_BOUND)
+
+        clocks = ClockSampler(gpu)
+        clocks.start()
+        t0, n = time.time(), 0
+        while n < 3 or time.time() - t0 < 0.5:
+            step()
+            torch.cuda.synchronize()
+            n += 1
+        fb_rows, fb_units, dev_status = bsattn.bsattn_query_stats(lay, stream)
+        bound_units, online_units = bsattn.bsattn_query_eligibility(lay, stream)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
+        t1 = time.time()
+        evs[0].record(stream)
+        for i in range(steps):
+            step(evs[2 * i + 1])
+            evs[2 * i + 2].record(stream)
+        torch.cuda.synchronize()
+        t2 = time.time()
+        ms_step = evs[0].elapsed_time(evs[-1]) / steps
+        fwd_ms = float(np.mean([evs[2 * i + 1].elapsed_time(evs[2 * i + 2]) for i in range(steps)]))
+        n_blk = max(5, int(0.25 / max(ms_step * 1e-3, 1e-4)))
+        ab = {}
+        for mode, fl in (("bound", bsattn.BSATTN_BOUND), ("online", bsattn.BSATTN_ONLINE_MAX)):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n_blk)]
+            a0 = time.time()
+            for a, b in ev:
+                a.record(stream)
+                fwd(fl)
+                b.record(stream)
+            torch.cuda.synchronize()
+            ab[mode] = (float(np.mean([a.elapsed_time(b) for a, b in ev])), a0, time.time())
+        clocks.stop()
+        clk = clocks.region(t1, t2)
+        mhz = {m: clocks.region(a0, a1)["sm_mhz"] for m, (_, a0, a1) in ab.items()}
+        value = flop / (ms_step * 1e-3) / 1e12
+        bm, om = ab["bound"][0], ab["online"][0]
+        out[name] = {
+            "useful_flop_per_step": flop, "ms_per_step": ms_step, "value": value, "unit": UNIT,
+            "pct_of_tensor_peak": 100.0 * value / peak, "forward_ms": fwd_ms,
+            "forward_tflops": flop / (fwd_ms * 1e-3) / 1e12, "clocks": clk,
+            "ab": {"bound_fwd_ms": bm, "bound_sm_mhz": mhz["bound"], "online_max_fwd_ms": om,
+                   "online_sm_mhz": mhz["online"], "bound_speedup_vs_online": om / bm,
+                   "bound_speedup_at_equal_clock": ((om * mhz["online"]) / (bm * mhz["bound"])
+                                                    if mhz["bound"] and mhz["online"] else None)},
+            "guard": {"fallback_rows": fb_rows, "fallback_units": fb_units, "device_status": dev_status},
+            "eligibility": {"bound_units": bound_units, "online_units": online_units}}
+        lay.destroy()
+        del o, qn, km, rb, dq
+    return out
 
 
 def mma_work(bsattn, lay) -> int:
