@@ -341,8 +341,9 @@ def main():
     bound_mhz, online_mhz = region_mhz(ab_win["bound"]), region_mhz(ab_win["online"])
     fwd_avg = float(np.mean(fwd_live))
     peaks, peak_src = _peaks()
-    # the forward call inside the timed region: workspace memset, the bound-softmax kernel and the
-    # (empty unless rows were flagged) rerun launch; the kernel is > 99.9% of it by the ncu launch list
+    # the forward call inside the timed region: the counter clear, the eligibility check, the
+    # bound-softmax kernel and the (empty unless units were routed or rows flagged) online launch;
+    # the bound kernel is > 99.5% of it by the ncu launch list
     achieved = flop_step / (fwd_avg * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     traffic = None
