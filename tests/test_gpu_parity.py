@@ -381,7 +381,7 @@ def test_eligibility_check_on_a_streamed_chunk_with_per_head_masks(ba):
 def test_guard_fires_on_eligible_rows(ba):
     # A key 5x longer puts the bounds of the rows that read it between 22 and 64 nats (57 at most):
     # they stay on the bound path (eligible), and those whose best logit lies > 44 nats below the
-    # bound are flagged and rerun; the predicted count follows the 32-row grouping of the kernel.
+    # bound are flagged and rerun; the predicted count follows the work units the eligibility check routes.
     w = synth.WORKLOADS["tiny"]
     q, k, v = _scaled_key(w, 5.0)
     mask, bs, scale = w.block_mask(), w.block, w.scale
