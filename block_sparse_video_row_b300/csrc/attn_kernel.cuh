@@ -369,6 +369,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ CUtensorMap tm_qt, const AttnParams p) {
     using C = AttnCfg<D>;
+    // Launched as soon as the kernel before it on the stream (the eligibility check, or the bound
+    // launch for the online one) lets it: wait for that kernel's results before reading anything.
+    grid_dep_wait();
+    grid_dep_launch_next();
     // Positions of this launch: the bound launch walks the schedule unless the route kernel
     // sent every unit online; the fallback launch walks the schedule when it sent some
     // (base = n_units), then the guard's fallback list.
@@ -860,8 +864,8 @@ cudaError_t launch_fwd_instance(const CUtensorMap &tq, const CUtensorMap &tk, co
                                 const AttnParams &p, int n_ctas, cudaStream_t s) {
     CUtensorMap to, tqt;
     if (!encode_o_store_map(&to, p, D) || !encode_q_tail_map(&tqt, p, D)) return cudaErrorInvalidValue;
-    bsattn_fwd_kernel<D, ONLINE><<<n_ctas, kAttnThreads, AttnCfg<D>::SMEM, s>>>(tq, tk, tv, to, tqt, p);
-    return cudaGetLastError();
+    return launch_after_kernel(bsattn_fwd_kernel<D, ONLINE>, static_cast<unsigned>(n_ctas), kAttnThreads,
+                               AttnCfg<D>::SMEM, s, tq, tk, tv, to, tqt, p);
 }
 
 // The register split in the kernel is valid only if it launches with exactly

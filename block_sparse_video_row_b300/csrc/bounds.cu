@@ -19,6 +19,7 @@
 // coalesced loads; a 16-lane group covers one row, a warp two rows.  Q has L rows
 // per head and K L_kv (more than L for a streamed chunk reading context frames).
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bsv {
 
@@ -62,6 +63,7 @@ __device__ __forceinline__ float tree16(float s, unsigned mask) {
 // fewer query than key blocks), writes the norms of the same rows of Q.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) norms_kernel(const BoundsParams p) {
+    grid_dep_launch_next();  // the row-bound kernel may start launching
     constexpr int PER = D / 16;
     const int cpb = p.chunks_per_block;
     const int chunk = static_cast<int>(blockIdx.x % cpb);
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kNormThreads) norms_kernel(const BoundsParams 
 }
 
 __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsParams p) {
+    grid_dep_wait();  // the norms and kmax of the kernel before are complete
     const int cpb = p.chunks_per_block;
     const int chunk = static_cast<int>(blockIdx.x % cpb);
     const int64_t seg = blockIdx.x / cpb;  // (b*H + h) * nb + qb
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(kNormThreads) rowbound_kernel(const BoundsPara
 // block, one norm per thread, one atomic max per CTA.  Negative and NaN entries lose
 // every comparison against the running maximum, which starts at 0.
 __global__ void __launch_bounds__(kNormThreads) kmax_from_norms_kernel(const BoundsParams p, const float *knorm) {
+    grid_dep_launch_next();  // the row-bound kernel may start launching
     const int cpb = p.chunks_per_block;
     const int chunk = static_cast<int>(blockIdx.x % cpb);
     const int64_t seg = blockIdx.x / cpb;  // (b*H + h) * nbkv + kb
@@ -194,8 +198,7 @@ cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s) {
 
 cudaError_t launch_rowbound(const BoundsParams &p, cudaStream_t s) {
     const int64_t grid = static_cast<int64_t>(p.BH) * p.nb * p.chunks_per_block;
-    rowbound_kernel<<<static_cast<unsigned>(grid), kNormThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_after_kernel(rowbound_kernel, static_cast<unsigned>(grid), kNormThreads, 0, s, p);
 }
 
 int bounds_chunk_rows() { return kChunkRows; }

@@ -126,6 +126,26 @@ bool encode_q_tail_map(CUtensorMap *m, const AttnParams &p, int D);
 // The eligibility check of every schedule slot before the forward's two launches: a
 // unit with a row bound above p.elig_m is routed to the online-max launch; also
 // clears the per-slot guard flags and counts n_online / n_bound (zeroed before).
+// Launch a kernel that may start while the kernel before it on the stream is still running
+// (programmatic dependent launch).  Every such kernel executes grid_dep_wait() before it reads
+// or writes anything the previous kernel touches; launched after a memset or a copy, or on a
+// device without the feature, it is ordered as an ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_route(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_norms(const BoundsParams &p, int D, cudaStream_t s);
 cudaError_t launch_rowbound(const BoundsParams &p, cudaStream_t s);

@@ -13,12 +13,14 @@
 // per-slot arrays.  A slot whose unit fields are out of range is left to the bound
 // launch, whose device checks (when on) reject and report it.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bsv {
 
 constexpr int kRouteThreads = 256;
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const AttnParams p) {
+    grid_dep_launch_next();  // the bound launch may start launching (it waits for this kernel)
     const int64_t slot = (static_cast<int64_t>(blockIdx.x) * kRouteThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (slot >= p.n_units) return;  // whole warps leave together
