@@ -256,7 +256,10 @@ bsattn_status bsattn_row_bounds_from_norms(bsattn_layout_t lay, const float *qno
  * finite, and every work unit holding a flagged row is recomputed by that
  * online-max launch too, on the same stream (no host synchronisation).  The
  * launches: a counter clear, the check, the bound kernel and the online-max
- * kernel; each exits at once when it has nothing to do.
+ * kernel; each exits at once when it has nothing to do.  The bound and
+ * online-max kernels are programmatic dependent launches: each may be scheduled
+ * while the kernel before it runs, and waits for that kernel's completion before
+ * it reads or writes anything, so stream order holds as for plain launches.
  * Enqueued on `stream`; returns BSATTN_OK, INVALID_ARG or CUDA.
  */
 bsattn_status bsattn_forward(bsattn_layout_t lay, const void *q, const void *k, const void *v, void *o,
