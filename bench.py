@@ -85,9 +85,17 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
+        self.samples = self.parse(self.path)
+        return self.samples
+
+    @staticmethod
+    def parse(path: str) -> list:
+        """Samples of an nvidia-smi CSV in FIELDS order: (time, sm MHz, max MHz, power W or None,
+        set of active throttle reasons); malformed lines are skipped."""
         import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        samples = []
+        for line in open(path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 10:
                 continue
@@ -98,8 +106,8 @@ class ClockSampler:
             except ValueError:
                 continue
             reasons = {n for n, val in zip(names, parts[6:10]) if val.lower() == "active"}
-            self.samples.append((ts, sm, smax, pw, reasons))
-        return self.samples
+            samples.append((ts, sm, smax, pw, reasons))
+        return samples
 
     def region(self, t0: float, t1: float) -> dict:
         """Median SM clock, max clock, median power and the throttle reasons seen in [t0, t1]."""
